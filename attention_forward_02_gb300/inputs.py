@@ -1,0 +1,73 @@
+"""Seeded synthetic inputs for the attention forward workloads.
+
+This module only draws and rounds random numbers; it holds none of the
+attention arithmetic.  The tests, the smoke check and the bench take their
+inputs from here, so the CUDA path and the fp64 oracle read identical values.
+
+Recipe: Q, K, V are iid N(0, 1) drawn in fp32 by ``torch.Generator`` (CPU,
+``manual_seed(seed)``; one seed per tensor), then rounded to the workload's
+16-bit dtype.  The stress variant multiplies the rounded Q by 8 (a power of
+two, so the product is exact in fp16/bf16), which spreads the scaled scores to
+a standard deviation of about 8 so that the running max keeps moving.
+
+Shapes follow the pages' [B, H, N, d] notation (contiguous, row stride d):
+"Triton으로 FlashAttention 1·2 forward 구현하기", section "기준 shape", uses
+[4, 32, 2048, 64] in fp16, and section "batch 크기에 따른 변화" varies B.
+"""
+import numpy as np
+import torch
+
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+# name -> (B, H, N, d, dtype, (seed_q, seed_k, seed_v))
+WORKLOADS = {
+    "tiny": (1, 2, 256, 64, "fp16", (0, 1, 2)),
+    "base": (4, 32, 2048, 64, "fp16", (10, 11, 12)),
+    "sweep_b1": (1, 32, 2048, 64, "fp16", (21, 22, 23)),
+    "sweep_b2": (2, 32, 2048, 64, "fp16", (24, 25, 26)),
+    "sweep_b4": (4, 32, 2048, 64, "fp16", (27, 28, 29)),
+    "sweep_b8": (8, 32, 2048, 64, "fp16", (50, 51, 52)),
+    "d128": (2, 16, 8192, 128, "bf16", (30, 31, 32)),
+    "long": (1, 8, 65536, 128, "fp16", (40, 41, 42)),
+}
+# seed of the query rows the oracle checks on the long-context workload
+LONG_ROW_SAMPLE_SEED = 43
+LONG_ROWS_PER_HEAD = 512
+
+
+def torch_dtype(name):
+    try:
+        return DTYPES[name]
+    except KeyError:
+        raise ValueError("dtype must be one of %s, got %r" % (sorted(DTYPES), name))
+
+
+def make_qkv(B, H, N, d, dtype="fp16", seeds=(0, 1, 2), q_scale=1.0):
+    """Return CPU tensors (q, k, v) of shape [B, H, N, d] in the 16-bit dtype."""
+    dt = torch_dtype(dtype) if isinstance(dtype, str) else dtype
+    out = []
+    for t, seed in enumerate(seeds):
+        g = torch.Generator(device="cpu").manual_seed(int(seed))
+        x = torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(dt)
+        if t == 0 and q_scale != 1.0:
+            x = x * q_scale
+        out.append(x.contiguous())
+    return tuple(out)
+
+
+def make_workload(name, q_scale=1.0):
+    """(q, k, v, meta) for a named workload; meta holds B, H, N, d, dtype."""
+    B, H, N, d, dtype, seeds = WORKLOADS[name]
+    q, k, v = make_qkv(B, H, N, d, dtype, seeds, q_scale=q_scale)
+    return q, k, v, dict(B=B, H=H, N=N, d=d, dtype=dtype)
+
+
+def sample_rows(B, H, N, per_head, seed):
+    """Seeded (bh, i) query-row sample: ``per_head`` distinct rows per head."""
+    rng = np.random.default_rng(int(seed))
+    rows = []
+    per = min(per_head, N)
+    for bh in range(B * H):
+        idx = np.sort(rng.choice(N, size=per, replace=False))
+        rows.extend((bh, int(i)) for i in idx)
+    return np.array(rows, dtype=np.int64).reshape(-1, 2)

@@ -1,0 +1,353 @@
+/*
+ * attention_oracle.c -- plain fp64 CPU oracle for the attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file: only the tests, the smoke check and the bench's CPU-baseline leg
+ * do.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (for every head (b,h) and query row i, keys j):
+ *
+ *   s_j   = scale * <q_i, k_j>                       for the allowed keys j
+ *   m     = max_j s_j
+ *   l     = sum_j exp(s_j - m)
+ *   o_i   = (sum_j exp(s_j - m) * v_j) / l
+ *   lse_i = m + ln(l)
+ *
+ * The allowed keys are all j (non-causal) or j <= i (causal).
+ *
+ * Sources (page title, section):
+ *  - "FlashAttention-2를 CuTe로 밑바닥부터 구현하며 겪은 GPU 커널 지옥기",
+ *    section "커널 구조는 단순한데, 디테일이 지옥임": the attention formula
+ *    (scores = QK^T / sqrt(d_h), row softmax, times V).
+ *  - "3.6 어텐션 I — 메모리 문제·FlashAttention 원리", section 3.6.4: the
+ *    max-shifted (stable) softmax and the online recurrence in the state
+ *    (m, l, O) with alpha = exp(m_old - m_new), normalised once at the end.
+ *  - same page, section 3.6.6: causal masking skips keys j > i.
+ *  - same page, section 3.6.7: the saved row statistic L = m + log(l),
+ *    read here as the natural logarithm over the scaled scores.
+ *
+ * Two entry families:
+ *  - oracle_attention_rows / oracle_attention_fwd: the plain definition,
+ *    computed two-pass per row (max first, then the sums).  Because the
+ *    tiled online method reaches this same result exactly (section 3.6.4
+ *    states that it is exact, not an approximation), this plain definition
+ *    is what the GPU path is compared against.
+ *  - oracle_online_row: the online recurrence of section 3.6.4, applied to
+ *    one row of scores split into caller-chosen blocks processed in a
+ *    caller-chosen order.  It records the state after every block so the
+ *    tests can check the page's hand-worked intermediate values
+ *    (section 3.6.5) and the block-order independence the page claims.
+ *
+ * Every function here is pinned by tests under tests/ (worked example,
+ * exercise, closed forms, invariants, source mutations).
+ *
+ * Arithmetic: IEEE fp64, evaluated in source order (built without
+ * fast-math, so the compiler does not reassociate the sums).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_ENOMEM 2
+
+/* Scores of query row i against the first n_keys keys of one head.
+ * q, k point at the head's [N, d] blocks (row-major). */
+static void scores_row(const double *q, const double *k, long i, long n_keys,
+                       long d, double scale, double *s)
+{
+    for (long j = 0; j < n_keys; ++j) {
+        double dot = 0.0;
+        for (long c = 0; c < d; ++c)
+            dot += q[i * d + c] * k[j * d + c];
+        s[j] = scale * dot;
+    }
+}
+
+/* Number of keys query row i may attend to (causal: keys 0..i). */
+static long allowed_keys(long i, long n, int causal)
+{
+    if (causal)
+        return i + 1;
+    return n;
+}
+
+/* Plain definition for one row: stable softmax of the scores, times V. */
+static void attention_row(const double *q, const double *k, const double *v,
+                          long i, long n, long d, double scale, int causal,
+                          double *s, double *o_i, double *lse_i)
+{
+    long n_keys = allowed_keys(i, n, causal);
+    scores_row(q, k, i, n_keys, d, scale, s);
+
+    double m = -INFINITY;
+    for (long j = 0; j < n_keys; ++j)
+        if (s[j] > m)
+            m = s[j];
+
+    double l = 0.0;
+    for (long j = 0; j < n_keys; ++j)
+        l += exp(s[j] - m);
+
+    for (long c = 0; c < d; ++c)
+        o_i[c] = 0.0;
+    for (long j = 0; j < n_keys; ++j) {
+        double p = exp(s[j] - m);
+        for (long c = 0; c < d; ++c)
+            o_i[c] += p * v[j * d + c];
+    }
+    for (long c = 0; c < d; ++c)
+        o_i[c] = o_i[c] / l;
+
+    *lse_i = m + log(l);
+}
+
+/* ------------------------------------------------------------------ */
+/* Threaded driver over a list of (head, row) pairs.                    */
+
+typedef struct {
+    const double *q, *k, *v;
+    const long *rows; /* pairs: head index bh, query index i */
+    long nrows, n, d;
+    double scale;
+    int causal;
+    double *o, *lse;
+    long begin, end;
+    int status;
+} row_job;
+
+static void *row_worker(void *arg)
+{
+    row_job *job = (row_job *)arg;
+    double *s = (double *)malloc((size_t)(job->n > 0 ? job->n : 1) * sizeof(double));
+    if (!s) {
+        job->status = ORACLE_ENOMEM;
+        return NULL;
+    }
+    long head_elems = job->n * job->d;
+    for (long r = job->begin; r < job->end; ++r) {
+        long bh = job->rows[2 * r];
+        long i = job->rows[2 * r + 1];
+        const double *qh = job->q + bh * head_elems;
+        const double *kh = job->k + bh * head_elems;
+        const double *vh = job->v + bh * head_elems;
+        attention_row(qh, kh, vh, i, job->n, job->d, job->scale, job->causal, s,
+                      job->o + r * job->d, job->lse + r);
+    }
+    free(s);
+    job->status = ORACLE_OK;
+    return NULL;
+}
+
+/*
+ * oracle_attention_rows: the plain definition for selected rows.
+ *   q, k, v : [BH, N, d] fp64, contiguous (BH = batch * heads)
+ *   rows    : nrows pairs (bh, i), 0 <= bh < BH, 0 <= i < N
+ *   o       : [nrows, d] fp64 output, lse : [nrows] fp64 output
+ *   nthreads: worker threads (<= 0 means 1)
+ * Returns 0 on success, 1 on an invalid argument, 2 when out of memory.
+ */
+int oracle_attention_rows(const double *q, const double *k, const double *v,
+                          long BH, long N, long d, double scale, int causal,
+                          const long *rows, long nrows, double *o, double *lse,
+                          int nthreads)
+{
+    if (BH < 0 || N < 0 || d < 1 || nrows < 0 || (causal != 0 && causal != 1))
+        return ORACLE_EINVAL;
+    if (nrows == 0)
+        return ORACLE_OK;
+    if (!q || !k || !v || !rows || !o || !lse || N == 0 || BH == 0)
+        return ORACLE_EINVAL;
+    for (long r = 0; r < nrows; ++r) {
+        if (rows[2 * r] < 0 || rows[2 * r] >= BH || rows[2 * r + 1] < 0 ||
+            rows[2 * r + 1] >= N)
+            return ORACLE_EINVAL;
+    }
+    if (nthreads <= 0)
+        nthreads = 1;
+    if (nthreads > nrows)
+        nthreads = (int)nrows;
+
+    row_job *jobs = (row_job *)calloc((size_t)nthreads, sizeof(row_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    unsigned char *spawned = (unsigned char *)calloc((size_t)nthreads, 1);
+    if (!jobs || !tids || !spawned) {
+        free(jobs);
+        free(tids);
+        free(spawned);
+        return ORACLE_ENOMEM;
+    }
+    long per = (nrows + nthreads - 1) / nthreads;
+    int status = ORACLE_OK;
+    for (int t = 0; t < nthreads; ++t) {
+        row_job *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v; jb->rows = rows; jb->nrows = nrows;
+        jb->n = N; jb->d = d; jb->scale = scale; jb->causal = causal;
+        jb->o = o; jb->lse = lse;
+        jb->begin = t * per;
+        jb->end = (t + 1) * per < nrows ? (t + 1) * per : nrows;
+        jb->status = ORACLE_OK;
+        if (jb->begin >= jb->end)
+            continue;
+        /* the last slice, or one whose thread failed to start, runs here */
+        if (t < nthreads - 1 && pthread_create(&tids[t], NULL, row_worker, jb) == 0)
+            spawned[t] = 1;
+        else
+            row_worker(jb);
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (spawned[t])
+            pthread_join(tids[t], NULL);
+        if (jobs[t].status != ORACLE_OK)
+            status = jobs[t].status;
+    }
+    free(spawned);
+    free(jobs);
+    free(tids);
+    return status;
+}
+
+/*
+ * oracle_attention_fwd: the plain definition for every row of every head.
+ *   q, k, v, o : [BH, N, d] fp64 contiguous; lse : [BH, N] fp64.
+ */
+int oracle_attention_fwd(const double *q, const double *k, const double *v,
+                         long BH, long N, long d, double scale, int causal,
+                         double *o, double *lse, int nthreads)
+{
+    if (BH < 0 || N < 0 || d < 1)
+        return ORACLE_EINVAL;
+    long nrows = BH * N;
+    if (nrows == 0)
+        return ORACLE_OK;
+    long *rows = (long *)malloc((size_t)nrows * 2 * sizeof(long));
+    if (!rows)
+        return ORACLE_ENOMEM;
+    for (long bh = 0; bh < BH; ++bh)
+        for (long i = 0; i < N; ++i) {
+            rows[2 * (bh * N + i)] = bh;
+            rows[2 * (bh * N + i) + 1] = i;
+        }
+    int st = oracle_attention_rows(q, k, v, BH, N, d, scale, causal, rows, nrows,
+                                   o, lse, nthreads);
+    free(rows);
+    return st;
+}
+
+/*
+ * oracle_scores_row: the scaled scores of query row i of one head against
+ * its allowed keys (all N, or 0..i when causal).  q, k: [N, d] fp64.
+ * s must hold N doubles; returns the number of scores written via *n_out.
+ */
+int oracle_scores_row(const double *q, const double *k, long N, long d, long i,
+                      double scale, int causal, double *s, long *n_out)
+{
+    if (!q || !k || !s || !n_out || N < 1 || d < 1 || i < 0 || i >= N)
+        return ORACLE_EINVAL;
+    long n_keys = allowed_keys(i, N, causal);
+    scores_row(q, k, i, n_keys, d, scale, s);
+    *n_out = n_keys;
+    return ORACLE_OK;
+}
+
+/*
+ * oracle_online_row: the online-softmax recurrence ("3.6 어텐션 I",
+ * section 3.6.4) over one row of scores s[0..n) with values v [n, d].
+ *
+ * The row is cut into nblocks blocks; block t covers scores
+ * [block_start[t], block_start[t] + block_len[t]) and blocks are processed
+ * in the order given (any order; the blocks need not be sorted).  State
+ * starts at m = -inf, l = 0, O = 0.  For every block:
+ *     m_tilde = max of the block's scores
+ *     m_new   = max(m, m_tilde)
+ *     alpha   = exp(m - m_new)          (0 on the first block: exp(-inf))
+ *     p_j     = exp(s_j - m_new)        for the block's scores
+ *     l       = alpha * l + sum_j p_j
+ *     O       = alpha * O + sum_j p_j * v_j
+ *     m       = m_new
+ * and at the end o = O / l.
+ *
+ * Outputs: o_out [d] (normalised), *l_out, *m_out.  If trace is not NULL it
+ * receives, per processed block, (m_tilde, m_new, alpha, l, O[0..d)) with O
+ * unnormalised: nblocks * (4 + d) doubles.
+ * The blocks must cover every score exactly once; otherwise returns 1.
+ */
+int oracle_online_row(const double *s, const double *v, long n, long d,
+                      const long *block_start, const long *block_len,
+                      long nblocks, double *o_out, double *l_out, double *m_out,
+                      double *trace)
+{
+    if (!s || !v || !block_start || !block_len || !o_out || !l_out || !m_out ||
+        n < 1 || d < 1 || nblocks < 1)
+        return ORACLE_EINVAL;
+    unsigned char *seen = (unsigned char *)calloc((size_t)n, 1);
+    double *acc = (double *)calloc((size_t)d, sizeof(double));
+    if (!seen || !acc) {
+        free(seen);
+        free(acc);
+        return ORACLE_ENOMEM;
+    }
+    int status = ORACLE_OK;
+    for (long t = 0; t < nblocks && status == ORACLE_OK; ++t) {
+        if (block_len[t] < 1 || block_start[t] < 0 || block_start[t] + block_len[t] > n) {
+            status = ORACLE_EINVAL;
+            break;
+        }
+        for (long j = block_start[t]; j < block_start[t] + block_len[t]; ++j) {
+            if (seen[j])
+                status = ORACLE_EINVAL;
+            seen[j] = 1;
+        }
+    }
+    for (long j = 0; j < n && status == ORACLE_OK; ++j)
+        if (!seen[j])
+            status = ORACLE_EINVAL;
+    if (status != ORACLE_OK) {
+        free(seen);
+        free(acc);
+        return status;
+    }
+
+    double m = -INFINITY;
+    double l = 0.0;
+    for (long t = 0; t < nblocks; ++t) {
+        long j0 = block_start[t], j1 = block_start[t] + block_len[t];
+        double m_tilde = -INFINITY;
+        for (long j = j0; j < j1; ++j)
+            if (s[j] > m_tilde)
+                m_tilde = s[j];
+        double m_new = m > m_tilde ? m : m_tilde;
+        double alpha = exp(m - m_new);
+        double block_sum = 0.0;
+        for (long j = j0; j < j1; ++j)
+            block_sum += exp(s[j] - m_new);
+        l = alpha * l + block_sum;
+        for (long c = 0; c < d; ++c) {
+            double pv = 0.0;
+            for (long j = j0; j < j1; ++j)
+                pv += exp(s[j] - m_new) * v[j * d + c];
+            acc[c] = alpha * acc[c] + pv;
+        }
+        m = m_new;
+        if (trace) {
+            double *tr = trace + t * (4 + d);
+            tr[0] = m_tilde;
+            tr[1] = m_new;
+            tr[2] = alpha;
+            tr[3] = l;
+            for (long c = 0; c < d; ++c)
+                tr[4 + c] = acc[c];
+        }
+    }
+    for (long c = 0; c < d; ++c)
+        o_out[c] = acc[c] / l;
+    *l_out = l;
+    *m_out = m;
+    free(seen);
+    free(acc);
+    return ORACLE_OK;
+}
+
+int oracle_abi_version(void) { return 1; }
