@@ -1,0 +1,63 @@
+"""GB300-native (sm_103a) FlashAttention-2 style attention forward.
+
+``fa_fwd(q, k, v, ...)`` computes O = softmax(Q K^T * scale) V and the row
+log-sum-exp for contiguous [B, H, N, d] fp16/bf16 CUDA tensors by calling the
+C ABI (include/fa.h) of the in-tree CUDA library on the current torch stream.
+PyTorch only supplies device memory and the stream; every step of the
+computation runs in the library's kernel.  There is no CPU or eager fallback:
+without the built library, or off a CUDA device, calls raise ``FAError``.
+"""
+from ._lib import (FA_BF16, FA_FP16, FAError, fa_abi_version, fa_fwd_raw,
+                   fa_last_device_status, fa_status_str, lib_path, load)
+
+__all__ = ["fa_fwd", "fa_fwd_raw", "fa_last_device_status", "fa_status_str", "fa_abi_version",
+           "FAError", "load", "lib_path"]
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float16:
+        return FA_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise FAError(2, "dtype must be float16 or bfloat16, got %s" % t.dtype)
+
+
+def fa_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, return_lse=True, stream=None):
+    """Attention forward on CUDA tensors q, k, v of shape [B, H, N, d].
+
+    o / lse: optional preallocated outputs ([B,H,N,d] in q's dtype and
+    [B,H,N] fp32); allocated with torch when None (lse only if return_lse).
+    scale defaults to 1/sqrt(d).  Returns (o, lse) (lse None if not requested).
+    The call is asynchronous on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise FAError(1, "%s must be a CUDA tensor" % name)
+        if t.dim() != 4 or not t.is_contiguous():
+            raise FAError(1, "%s must be a contiguous [B, H, N, d] tensor" % name)
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise FAError(1, "q, k, v must share shape and dtype")
+    B, H, N, d = q.shape
+    code = _dtype_code(q)
+    if scale is None:
+        scale = float(d) ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    elif o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous() or not o.is_cuda:
+        raise FAError(1, "o must be a contiguous CUDA tensor shaped and typed like q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    if lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32
+                            or not lse.is_contiguous() or not lse.is_cuda):
+        raise FAError(1, "lse must be a contiguous CUDA float32 tensor of shape [B, H, N]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                        lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
+                        int(bool(causal)), code, stream.cuda_stream)
+    if st != 0:
+        raise FAError(st, "fa_fwd")
+    return o, lse

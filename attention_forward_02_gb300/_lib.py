@@ -1,0 +1,81 @@
+"""ctypes binding of the C ABI in include/fa.h (argument marshalling only).
+
+The shared library is built in-tree by ``attention_forward_02_gb300.build``.
+There is no fallback: if the library is missing or fails to load, every call
+raises ``FAError``.
+"""
+import ctypes
+import os
+
+from .build import LIB
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+FA_FP16 = 0
+FA_BF16 = 1
+
+# every symbol include/fa.h declares
+EXPORTS = ("fa_fwd", "fa_last_device_status", "fa_status_str", "fa_abi_version")
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = int(status)
+        name = status_name(status)
+        super().__init__("%s%s" % (name, (": " + what) if what else ""))
+
+
+def status_name(status):
+    names = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
+             4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+    return names.get(int(status), "FA_ERR_UNKNOWN(%d)" % int(status))
+
+
+def load(path=None):
+    """Load (once) and return the CUDA library; raise if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB
+    if not os.path.exists(path):
+        raise FAError(FA_ERR_CUDA, "CUDA library %s is not built; run "
+                      "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.restype = i
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.fa_last_device_status.restype = i
+    lib.fa_last_device_status.argtypes = [vp]
+    lib.fa_status_str.restype = ctypes.c_char_p
+    lib.fa_status_str.argtypes = [i]
+    lib.fa_abi_version.restype = i
+    lib.fa_abi_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def lib_path():
+    return LIB
+
+
+def fa_fwd_raw(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream):
+    """Direct call of the C entry point with integer pointers; returns the status."""
+    return load().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream)
+
+
+def fa_last_device_status(stream=None):
+    return load().fa_last_device_status(stream)
+
+
+def fa_status_str(status):
+    return load().fa_status_str(int(status)).decode()
+
+
+def fa_abi_version():
+    return load().fa_abi_version()

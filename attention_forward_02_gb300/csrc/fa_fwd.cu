@@ -1,0 +1,220 @@
+// fa_fwd.cu -- host side of the C ABI declared in include/fa.h: argument
+// checks, TMA descriptor encoding, and the launch of the sm_103a kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::once_flag once;
+    fa_status_t init_status = FA_ERR_CUDA;
+    EncodeTiledFn encode = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+template <int D, bool CAUSAL, typename T>
+cudaError_t set_smem_attr()
+{
+    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, T>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, fa::KCfg<D>::SMEM_ALLOC);
+}
+
+void init_device(int dev, DeviceState &st)
+{
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+        st.init_status = FA_ERR_CUDA;
+        return;
+    }
+    // tcgen05 / TMEM kernels are built for sm_103a only.
+    if (prop.major != 10 || prop.minor != 3) {
+        st.init_status = FA_ERR_UNSUPPORTED;
+        return;
+    }
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        st.init_status = FA_ERR_CUDA;
+        return;
+    }
+    st.encode = reinterpret_cast<EncodeTiledFn>(fn);
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = set_smem_attr<64, false, __half>();
+    if (e == cudaSuccess) e = set_smem_attr<64, true, __half>();
+    if (e == cudaSuccess) e = set_smem_attr<128, false, __half>();
+    if (e == cudaSuccess) e = set_smem_attr<128, true, __half>();
+    if (e == cudaSuccess) e = set_smem_attr<64, false, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr<64, true, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr<128, false, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr<128, true, __nv_bfloat16>();
+    st.init_status = (e == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t device_state(DeviceState **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FA_ERR_CUDA;
+    DeviceState &st = g_dev[dev];
+    std::call_once(st.once, init_device, dev, std::ref(st));
+    *out = &st;
+    return st.init_status;
+}
+
+// 3-D view [BH, N, d] of a contiguous [B, H, N, d] tensor; box = 64 columns
+// (128 bytes, one swizzle span) x 128 rows x 1 head, SWIZZLE_128B, rows past N
+// read as zeros.
+fa_status_t encode_qkv_map(EncodeTiledFn encode, CUtensorMap *map, const void *ptr, int BH, int N,
+                           int d, fa_dtype_t dtype)
+{
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map,
+                        dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, bool CAUSAL, typename T>
+fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
+                   float *lse, int BH, int N, float scale, cudaStream_t stream)
+{
+    const int num_q_tiles = (N + fa::kBM - 1) / fa::kBM;
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(num_q_tiles));
+    fa::fa_fwd_kernel<D, CAUSAL, T><<<grid, fa::kNumThreads, fa::KCfg<D>::SMEM_ALLOC, stream>>>(
+        mq, mk, mv, static_cast<T *>(o), lse, N, num_q_tiles, scale, scale_log2);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+bool overlaps(uintptr_t a, size_t na, uintptr_t b, size_t nb) { return a < b + nb && b < a + na; }
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int N, int d, float scale, int causal, fa_dtype_t dtype, void *stream)
+{
+    // ---- argument checks (no CUDA call before they pass) ----
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1)
+        return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale))
+        return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16)
+        return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;
+    if (scale < 0.f)
+        return FA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0)
+        return FA_OK;  // empty problem
+    if (!q || !k || !v || !o)
+        return FA_ERR_INVALID_ARG;
+    const long long BH = static_cast<long long>(B) * H;
+    if (BH > 0x7fffffffLL)
+        return FA_ERR_UNSUPPORTED;
+    if ((N + fa::kBM - 1) / fa::kBM > 65535)
+        return FA_ERR_UNSUPPORTED;  // grid.y limit
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 15u)
+        return FA_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u)
+        return FA_ERR_MISALIGNED;
+    const size_t bytes = static_cast<size_t>(BH) * N * d * 2;
+    const uintptr_t uo = reinterpret_cast<uintptr_t>(o);
+    if (overlaps(uo, bytes, reinterpret_cast<uintptr_t>(q), bytes) ||
+        overlaps(uo, bytes, reinterpret_cast<uintptr_t>(k), bytes) ||
+        overlaps(uo, bytes, reinterpret_cast<uintptr_t>(v), bytes))
+        return FA_ERR_INVALID_ARG;
+    if (lse) {
+        const size_t lbytes = static_cast<size_t>(BH) * N * sizeof(float);
+        const uintptr_t ul = reinterpret_cast<uintptr_t>(lse);
+        if (overlaps(ul, lbytes, uo, bytes) || overlaps(ul, lbytes, reinterpret_cast<uintptr_t>(q), bytes) ||
+            overlaps(ul, lbytes, reinterpret_cast<uintptr_t>(k), bytes) ||
+            overlaps(ul, lbytes, reinterpret_cast<uintptr_t>(v), bytes))
+            return FA_ERR_INVALID_ARG;
+    }
+
+    // ---- device state, descriptors, launch ----
+    DeviceState *st = nullptr;
+    fa_status_t s = device_state(&st);
+    if (s != FA_OK)
+        return s;
+    CUtensorMap mq, mk, mv;
+    const int bh = static_cast<int>(BH);
+    if ((s = encode_qkv_map(st->encode, &mq, q, bh, N, d, dtype)) != FA_OK) return s;
+    if ((s = encode_qkv_map(st->encode, &mk, k, bh, N, d, dtype)) != FA_OK) return s;
+    if ((s = encode_qkv_map(st->encode, &mv, v, bh, N, d, dtype)) != FA_OK) return s;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (dtype == FA_FP16) {
+        if (d == 64)
+            return causal ? launch<64, true, __half>(mq, mk, mv, o, lse, bh, N, scale, cs)
+                          : launch<64, false, __half>(mq, mk, mv, o, lse, bh, N, scale, cs);
+        return causal ? launch<128, true, __half>(mq, mk, mv, o, lse, bh, N, scale, cs)
+                      : launch<128, false, __half>(mq, mk, mv, o, lse, bh, N, scale, cs);
+    }
+    if (d == 64)
+        return causal ? launch<64, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs)
+                      : launch<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs);
+    return causal ? launch<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs)
+                  : launch<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs);
+}
+
+fa_status_t fa_last_device_status(void *stream)
+{
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(cs) != cudaSuccess)
+        return FA_ERR_CUDA;
+    unsigned int word = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(&word, fa::g_fa_status, sizeof(word)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return (word & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+const char *fa_status_str(fa_status_t status)
+{
+    switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+int fa_abi_version(void) { return FA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Benchmark: attention forward TFLOP/s on one GB300 (and % of dense tensor peak).
+
+One step = one pass of the whole hot path over one batch: the tiled online-
+softmax attention forward on the workload, non-causal then causal (the two
+variants the base configuration names), FLOPs = 4*B*H*N^2*d each, halved for
+causal.  Default workload: B=4, H=32, N=2048, d=64, fp16, scale 1/sqrt(64),
+seeded iid N(0,1) inputs ("base").
+
+Prints ONE JSON line (rank 0).  Keys beyond the metric: roofline (dominant
+kernel = the non-causal launch), cpu_baseline (the fp64 oracle on host cores,
+bounded row sample), e2e (pinned host buffers, H2D + compute + D2H per step),
+clocks (nvidia-smi sampled during warm-up + timed region), gpu_launches.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build)
+on a bounded row sample of the same workload, on the host cores.
+
+Multi-GPU (torchrun): each rank runs its own copy of the workload on its own
+GPU (weak scaling; attention over (batch*head, Q tile) needs no exchange);
+time = max over ranks; value = all ranks' FLOPs / that time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="base")
+    ap.add_argument("--variants", default="noncausal,causal",
+                    help="comma list of noncausal/causal launches per step")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target host seconds for the cpu_baseline / reference sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def flops_of(meta, causal):
+    f = 4.0 * meta["B"] * meta["H"] * meta["N"] ** 2 * meta["d"]
+    return f / 2 if causal else f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload, src_hash):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, valid only while the kernel sources are the ones profiled."""
+    path = os.path.join(ROOT, "profiles", "fa_fwd_%s_dram.md" % workload)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, None
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != src_hash:
+        return None, path
+    return float(m_bytes.group(1)), path
+
+
+# ---------------------------------------------------------------------------
+# clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = (uuid or "").lower()
+        self.proc = None
+        self.lines = []
+        self.t_load = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_load(self, t0, t1):
+        self.t_load = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0, t1 = self.t_load or (0, float("inf"))
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and self.uuid not in parts[1].lower():
+                continue
+            if not (t0 <= ts <= t1):
+                continue
+            try:
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(dist, value, device=None):
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value, device=None):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+
+
+def oracle_sample_rows(meta, n_rows, seed=12345):
+    import numpy as np
+    B, H, N = meta["B"], meta["H"], meta["N"]
+    rng = np.random.default_rng(seed)
+    flat = rng.choice(B * H * N, size=min(n_rows, B * H * N), replace=False)
+    return np.stack([flat // N, flat % N], axis=1).astype(np.int64)
+
+
+def oracle_row_flops(meta, rows, causal):
+    import numpy as np
+    if causal:
+        return float(np.sum(4.0 * (rows[:, 1] + 1) * meta["d"]))
+    return 4.0 * len(rows) * meta["N"] * meta["d"]
+
+
+class OracleTimer:
+    """Times the fp64 oracle (as it stands) on row samples of the workload."""
+
+    def __init__(self, q, k, v, meta, variants):
+        import oracle
+        self.orc = oracle.get()
+        self.meta = meta
+        self.variants = variants
+        self.q64 = q.double().numpy()
+        self.k64 = k.double().numpy()
+        self.v64 = v.double().numpy()
+        self.threads = self.orc.default_threads()
+        self.scale = meta["d"] ** -0.5
+
+    def run(self, rows):
+        t0 = time.perf_counter()
+        flops = 0.0
+        for causal in self.variants:
+            self.orc.attention_rows(self.q64, self.k64, self.v64, rows, self.scale, causal=causal,
+                                    threads=self.threads)
+            flops += oracle_row_flops(self.meta, rows, causal)
+        return time.perf_counter() - t0, flops
+
+    def rows_for_seconds(self, seconds):
+        """Calibrate: rows whose oracle time is about `seconds`."""
+        probe = oracle_sample_rows(self.meta, 2 * self.threads, seed=1)
+        dt, _ = self.run(probe)
+        per_row = max(dt / len(probe), 1e-7)
+        return max(1, int(seconds / per_row))
+
+
+def cpu_baseline_obj(timer, seconds, seed=99):
+    n = timer.rows_for_seconds(seconds)
+    rows = oracle_sample_rows(timer.meta, n, seed=seed)
+    dt, flops = timer.run(rows)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+            "sample": "%d random query rows of workload %s (of %d), variants %s, fp64 C oracle, "
+                      "%.1f s" % (len(rows), timer.meta["name"],
+                                   timer.meta["B"] * timer.meta["H"] * timer.meta["N"],
+                                   "+".join("causal" if c else "noncausal" for c in timer.variants),
+                                   dt)}
+
+
+# ---------------------------------------------------------------------------
+
+
+def main():
+    args = parse_args()
+    from attention_forward_02_gb300 import inputs
+
+    world, rank, local = dist_env()
+    variants = [v.strip() == "causal" for v in args.variants.split(",") if v.strip()]
+    q, k, v, meta = inputs.make_workload(args.workload)
+    meta["name"] = args.workload
+    config = {"workload": "%s B=%d H=%d N=%d d=%d %s" % (args.workload, meta["B"], meta["H"],
+                                                         meta["N"], meta["d"], meta["dtype"]),
+              "B": meta["B"], "H": meta["H"], "N": meta["N"], "d": meta["d"],
+              "scale": "1/sqrt(d)",
+              "variants": ["causal" if c else "noncausal" for c in variants],
+              "inputs": "seeded iid N(0,1), rounded to %s" % meta["dtype"],
+              "l2": "flushed between timed steps (256 MiB write)",
+              "parallelism": "dp%d (independent replicas)" % max(world, args.gpus)}
+    step_flops = sum(flops_of(meta, c) for c in variants)
+
+    if args.impl == "reference":
+        return run_reference(args, q, k, v, meta, variants, config, step_flops, world, rank)
+
+    import torch
+    import attention_forward_02_gb300 as fa
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product has no CPU path)")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    fa.load()
+
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    outs = [(torch.empty_like(qd), torch.empty((meta["B"], meta["H"], meta["N"]),
+                                               dtype=torch.float32, device=dev)) for _ in variants]
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = meta["d"] ** -0.5
+
+    def step():
+        for (o, lse), causal in zip(outs, variants):
+            fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    t_load0 = time.time()
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    st = fa.fa_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise SystemExit("device status after warm-up: %s" % fa.fa_status_str(st))
+
+    K = args.steps
+    nv = len(variants)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nv + 1)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(2_000_000)  # let the host run ahead so launches queue back to back
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, ((o, lse), causal) in enumerate(zip(outs, variants)):
+            fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    t_load1 = time.time()
+    sampler.mark_load(t_load0, t_load1)
+    st = fa.fa_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise SystemExit("device status after timed region: %s" % fa.fa_status_str(st))
+
+    step_ms = [ev[i][0].elapsed_time(ev[i][nv]) for i in range(K)]
+    per_kernel_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)] for j in range(nv)]
+    total_ms = max_over_ranks(dist, sum(step_ms), dev)
+    total_flops = sum_over_ranks(dist, step_flops * K, dev)
+    value = total_flops / (total_ms / 1e3) / 1e12
+    ms_per_step = total_ms / K
+
+    # e2e through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(fa, torch, q, k, v, meta, variants, dev, stream, scale, step_flops,
+                      max(3, min(K, 50)), dist)
+
+    clocks = sampler.stop()
+    peaks, peak_src = load_peaks()
+    dom = variants.index(False) if False in variants else 0  # the non-causal launch
+    dom_causal = variants[dom]
+    dom_ms = statistics.mean(per_kernel_ms[dom])
+    achieved = flops_of(meta, dom_causal) / (dom_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    src_hash = kernel_source_hash()
+    traffic, traffic_src = recorded_traffic(args.workload, src_hash)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "fa_fwd_kernel<%d,%s,%s>" % (meta["d"], "causal" if dom_causal else
+                                                       "noncausal", meta["dtype"]),
+                "peak_source": "%s bf16_tflops (burst; fp16 dense rate equals bf16)" % peak_src,
+                "launch_ms": dom_ms,
+                "algorithmic_flops_per_launch": flops_of(meta, dom_causal),
+                "variants_tflops": {("causal" if c else "noncausal"):
+                                    flops_of(meta, c) / (statistics.mean(per_kernel_ms[j]) / 1e3)
+                                    / 1e12 for j, c in enumerate(variants)}}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        timer = OracleTimer(q, k, v, meta, variants)
+        cpu = cpu_baseline_obj(timer, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "pct_of_peak": 100.0 * value / peak,
+                "dtype": meta["dtype"], "data": "synthetic", "config": config,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "gpu_launches": K * nv * 1, "wall_s_timed": t_wall}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(fa, torch, q, k, v, meta, variants, dev, stream, scale, step_flops, steps, dist):
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    qd, kd, vd = torch.empty_like(hq, device=dev), torch.empty_like(hk, device=dev), \
+        torch.empty_like(hv, device=dev)
+    houts = [(torch.empty_like(hq).pin_memory(),
+              torch.empty((meta["B"], meta["H"], meta["N"]), dtype=torch.float32).pin_memory())
+             for _ in variants]
+    douts = [(torch.empty_like(qd), torch.empty((meta["B"], meta["H"], meta["N"]),
+                                                dtype=torch.float32, device=dev)) for _ in variants]
+    h2d = 3 * hq.numel() * hq.element_size()
+    d2h = sum(o.numel() * o.element_size() + l.numel() * 4 for o, l in houts)
+
+    def one():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        for (o, l), (ho, hl), causal in zip(douts, houts, variants):
+            fa.fa_fwd(qd, kd, vd, o=o, lse=l, scale=scale, causal=causal, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(l, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        ms = max_over_ranks(dist, ms, dev)
+        flops = sum_over_ranks(dist, step_flops * steps, dev)
+    else:
+        flops = step_flops * steps
+    return {"value": flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+
+
+def run_reference(args, q, k, v, meta, variants, config, step_flops, world, rank):
+    """The reference arm: the fp64 CPU oracle, as it stands, on host cores."""
+    if rank != 0:
+        return
+    timer = OracleTimer(q, k, v, meta, variants)
+    budget = max(30.0, min(150.0, args.cpu_seconds * 8))
+    n_steps = args.steps + max(args.warmup, 0)
+    rows_per_step = max(1, timer.rows_for_seconds(budget / max(n_steps, 1)))
+    for i in range(max(args.warmup, 0)):
+        timer.run(oracle_sample_rows(meta, rows_per_step, seed=500 + i))
+    tot_t, tot_f = 0.0, 0.0
+    for i in range(args.steps):
+        dt, fl = timer.run(oracle_sample_rows(meta, rows_per_step, seed=1000 + i))
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = ("each step: %d random query rows of %s (of %d), variants %s, fp64 C oracle"
+              % (rows_per_step, args.workload, meta["B"] * meta["H"] * meta["N"],
+                 "+".join(config["variants"])))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": timer.threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

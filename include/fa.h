@@ -1,0 +1,107 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) attention-forward library.
+ *
+ * One operation: the FlashAttention-2 style tiled attention forward
+ *
+ *     O = softmax(Q K^T * scale) V,     LSE = log(sum_j exp(scale * q_i . k_j))
+ *
+ * computed per (batch, head) with an online softmax whose running max m,
+ * running sum l and unnormalised output accumulator stay on chip for the
+ * whole K/V loop; the N x N score matrix is never written to device memory.
+ *
+ * Sources (page title, section):
+ *  - "3.6 어텐션 I — 메모리 문제·FlashAttention 원리": 3.6.4 (online softmax
+ *    recurrence, alpha = exp(m_old - m_new), one final division by l), 3.6.6
+ *    (the FA2 tile loop: Q block outer / parallel, K/V blocks inner; causal
+ *    skips key blocks j > i and masks the diagonal block), 3.6.7 (row
+ *    statistic L = m + log l saved for the backward pass).
+ *  - "Triton으로 FlashAttention 1·2 forward 구현하기", section "병렬화 단위":
+ *    grid = (cdiv(N, BLOCK_M), B * H), one program per Q block.
+ *  - "FlashAttention-2를 CuTe로 밑바닥부터 구현하며 겪은 GPU 커널 지옥기",
+ *    section "커널 구조는 단순한데, 디테일이 지옥임": P = QK^T / sqrt(d_h).
+ *
+ * All functions are plain C, thread-safe, and never throw.  No torch or
+ * CUDA types appear in the signatures: device buffers are plain pointers and
+ * the stream is a cudaStream_t passed as void* (NULL = the legacy default
+ * stream of the calling thread's current device).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+/* Status codes.  Every entry point returns one of these. */
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* a NULL buffer, a negative size, causal not 0/1, a
+                               non-finite scale, overlapping output and input */
+    FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, negative scale, dtype unknown,
+                               N beyond the grid limit, device not sm_103 */
+    FA_ERR_MISALIGNED = 3,  /* q, k, v or o not 16-byte aligned; lse not 4-byte */
+    FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or the launch failed */
+    FA_ERR_TIMEOUT = 5      /* a kernel wait gave up (reported by
+                               fa_last_device_status after the stream drained) */
+} fa_status_t;
+
+/* Element type of Q, K, V and O (all four share it); accumulation is fp32. */
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
+
+/*
+ * fa_fwd -- attention forward on the caller's stream (asynchronous).
+ *
+ *  q, k, v : device pointers, contiguous [B, H, N, d] tensors of `dtype`
+ *            (row stride d elements), 16-byte aligned.  Read only.
+ *  o       : device pointer, contiguous [B, H, N, d] of `dtype`, 16-byte
+ *            aligned; must not overlap q, k or v.  Written: O rounded to
+ *            nearest from fp32.
+ *  lse     : device pointer to [B, H, N] fp32 (4-byte aligned), or NULL to
+ *            skip it.  Written: lse = m * scale + ln(l), the natural log of
+ *            sum_j exp(scale * q_i . k_j) over the allowed keys.
+ *  B, H, N : batch, heads, sequence length (queries = keys = N).  Any of them
+ *            0 is an empty problem: FA_OK, nothing launched.  Ragged N (not a
+ *            multiple of the 128-row tile) is supported.
+ *  d       : head dimension, 64 or 128.
+ *  scale   : score scale (1/sqrt(d) for standard attention); finite, >= 0.
+ *  causal  : 0 = every key; 1 = query i attends to keys j <= i.
+ *  dtype   : FA_FP16 or FA_BF16.
+ *  stream  : cudaStream_t (as void*), or NULL.
+ *
+ * Ownership: the caller owns every buffer; the library allocates no device
+ * memory.  Argument errors are detected before anything is launched and leave
+ * the outputs untouched.  A launch failure returns FA_ERR_CUDA.  A kernel
+ * whose internal wait times out finishes early, leaves O/LSE partially
+ * written, and records FA_ERR_TIMEOUT for fa_last_device_status.
+ */
+FA_API fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int N, int d, float scale, int causal,
+                   fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_last_device_status -- synchronise `stream`, read and clear the device
+ * status word of the current device.  Returns FA_ERR_TIMEOUT if any kernel
+ * launched since the last call gave up on a wait, FA_ERR_CUDA if the stream
+ * reports an error, else FA_OK.  Not for use during CUDA graph capture.
+ */
+FA_API fa_status_t fa_last_device_status(void *stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+FA_API const char *fa_status_str(fa_status_t status);
+
+/* FA_ABI_VERSION of the built library. */
+FA_API int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,87 @@
+"""The C-ABI library builds, loads and exports every symbol include/fa.h
+declares; argument errors are rejected before any CUDA call.  CPU only: no
+call here reaches a kernel launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_forward_02_gb300 as fa
+from attention_forward_02_gb300 import _lib
+from attention_forward_02_gb300.build import INCLUDE, build_library
+
+HEADER = os.path.join(INCLUDE, "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_abi_version_matches_header(lib):
+    m = re.search(r"#define FA_ABI_VERSION (\d+)", open(HEADER).read())
+    assert fa.fa_abi_version() == int(m.group(1))
+
+
+def test_status_strings(lib):
+    names = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
+             "FA_ERR_CUDA", "FA_ERR_TIMEOUT"]
+    for code, name in enumerate(names):
+        assert fa.fa_status_str(code) == name
+        assert _lib.status_name(code) == name
+    assert fa.fa_status_str(99) == "FA_ERR_UNKNOWN"
+
+
+# Fake, well-separated, 16-byte-aligned "device" addresses: every call below
+# must be rejected (or be an empty problem) before the library touches CUDA.
+Q, K, V, O, L = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def call(q=Q, k=K, v=V, o=O, lse=L, B=1, H=2, N=256, d=64, scale=0.125, causal=0, dtype=0):
+    return fa.fa_fwd_raw(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(d=96), 2), (dict(d=32), 2), (dict(d=256), 2),
+    (dict(dtype=7), 2), (dict(scale=-1.0), 2),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(causal=2), 1), (dict(B=-1), 1), (dict(N=-5), 1),
+    (dict(q=0), 1), (dict(o=0), 1),
+    (dict(q=Q + 2), 3), (dict(k=K + 8), 3), (dict(o=O + 4), 3), (dict(lse=L + 2), 3),
+    (dict(o=Q + 4096), 1),          # output overlaps q
+    (dict(lse=O + 64), 1),          # lse overlaps o
+    (dict(N=65535 * 128 + 1), 2),   # more Q tiles than the grid allows
+    (dict(N=0), 0), (dict(B=0), 0), (dict(H=0, q=0, o=0), 0),  # empty problems
+], ids=lambda x: str(x))
+def test_argument_checks(lib, kwargs, status):
+    assert call(**kwargs) == status
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(fa.FAError):
+        _lib.load(str(tmp_path / "missing.so"))
+
+
+def test_cpu_tensors_are_rejected():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 128, 64, dtype=torch.float16)
+    with pytest.raises(fa.FAError):
+        fa.fa_fwd(x, x, x)

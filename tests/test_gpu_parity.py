@@ -1,0 +1,143 @@
+"""CUDA path vs the fp64 oracle through the C ABI, on seeded inputs.
+
+Small shapes are compared element by element in full (several tiles and a
+ragged tail); the full-size workloads, in the launch configuration the bench
+times, are compared on seeded row samples plus the tile-edge rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_forward_02_gb300 import inputs
+from parity_util import check_full, check_rows, edge_rows, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return oracle.get()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_workload_full(orc, causal):
+    q, k, v, meta = inputs.make_workload("tiny")
+    scale = meta["d"] ** -0.5
+    o, lse = run_gpu(q, k, v, scale, causal)
+    check_full(orc, q, k, v, scale, causal, o, lse, "tiny causal=%s" % causal)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 7, 64, 127, 128, 129, 255, 256, 257, 383, 640])
+def test_ragged_lengths_full(orc, dtype, d, causal, N):
+    q, k, v = inputs.make_qkv(1, 2, N, d, dtype, (1000 + N, 2000 + N, 3000 + N))
+    scale = d ** -0.5
+    o, lse = run_gpu(q, k, v, scale, causal)
+    check_full(orc, q, k, v, scale, causal, o, lse, "N=%d d=%d %s causal=%s" % (N, d, dtype, causal))
+
+
+@pytest.mark.parametrize("d,dtype", [(64, "fp16"), (128, "bf16")])
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_head_multi_tile_full(orc, d, dtype, causal):
+    q, k, v = inputs.make_qkv(2, 3, 1000, d, dtype, (7, 8, 9))
+    scale = d ** -0.5
+    o, lse = run_gpu(q, k, v, scale, causal)
+    check_full(orc, q, k, v, scale, causal, o, lse, "B2H3N1000 d=%d" % d)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_stress_q_times_8_full(orc, causal):
+    """Q x 8: scaled scores with sd ~8, so the running max moves often and the
+    O rescale by alpha is exercised hard."""
+    q, k, v = inputs.make_qkv(1, 4, 2048, 64, "fp16", (61, 62, 63), q_scale=8.0)
+    scale = 64 ** -0.5
+    o, lse = run_gpu(q, k, v, scale, causal)
+    check_full(orc, q, k, v, scale, causal, o, lse, "stress causal=%s" % causal)
+
+
+def test_lse_optional_gives_same_output(orc):
+    q, k, v = inputs.make_qkv(1, 2, 300, 128, "fp16", (4, 5, 6))
+    o1, lse = run_gpu(q, k, v, 128 ** -0.5, True, with_lse=True)
+    o2, none = run_gpu(q, k, v, 128 ** -0.5, True, with_lse=False)
+    assert none is None
+    assert torch.equal(o1, o2)
+
+
+def test_deterministic(orc):
+    q, k, v = inputs.make_qkv(2, 4, 777, 64, "bf16", (11, 12, 13))
+    o1, l1 = run_gpu(q, k, v, 0.125, False)
+    o2, l2 = run_gpu(q, k, v, 0.125, False)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_scale_zero_is_mean_of_values(orc):
+    """Closed form on the GPU: scale 0 gives uniform weights."""
+    q, k, v = inputs.make_qkv(1, 2, 300, 64, "fp16", (14, 15, 16))
+    for causal in (False, True):
+        o, lse = run_gpu(q, k, v, 0.0, causal)
+        vd = v.double()
+        if causal:
+            ref = vd.cumsum(dim=2) / torch.arange(1, 301, dtype=torch.float64).view(1, 1, -1, 1)
+            lref = torch.log(torch.arange(1, 301, dtype=torch.float64)).view(1, 1, -1).expand(1, 2, 300)
+        else:
+            ref = vd.mean(dim=2, keepdim=True).expand_as(vd)
+            lref = torch.full((1, 2, 300), float(np.log(300)), dtype=torch.float64)
+        assert float((o.double().cpu() - ref).abs().max()) <= 2e-3 * float(v.abs().max())
+        assert float((lse.double().cpu() - lref).abs().max()) <= 1e-3
+
+
+def test_empty_problem_writes_nothing(orc):
+    import attention_forward_02_gb300 as fa
+    dev = torch.device("cuda:0")
+    x = torch.zeros(1, 1, 0, 64, dtype=torch.float16, device=dev)
+    o, lse = fa.fa_fwd(x, x, x)
+    assert o.shape == x.shape and lse.shape == (1, 1, 0)
+
+
+def test_status_errors_on_device(orc):
+    import attention_forward_02_gb300 as fa
+    dev = torch.device("cuda:0")
+    x = torch.zeros(1, 1, 256, 96, dtype=torch.float16, device=dev)
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_fwd(x, x, x)
+    assert e.value.status == 2
+    buf = torch.zeros(1 * 1 * 256 * 64 + 8, dtype=torch.float16, device=dev)
+    y = buf[1:1 + 256 * 64].view(1, 1, 256, 64)  # 2-byte offset: not 16-byte aligned
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_fwd(y, y, y)
+    assert e.value.status == 3
+    assert fa.fa_last_device_status(None) == 0
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads (bench launch configuration), sampled rows
+
+FULL = [("base", 1.0, 64), ("sweep_b1", 1.0, 32), ("sweep_b2", 1.0, 32), ("sweep_b4", 1.0, 16),
+        ("sweep_b8", 1.0, 8), ("sweep_b4", 8.0, 16), ("d128", 1.0, 128)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("name,q_scale,per_head", FULL, ids=["%s_q%g" % (n, s) for n, s, _ in FULL])
+def test_full_size_sampled(orc, name, q_scale, per_head, causal):
+    q, k, v, meta = inputs.make_workload(name, q_scale=q_scale)
+    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+    scale = d ** -0.5
+    o, lse = run_gpu(q, k, v, scale, causal)
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    rows = edge_rows(B, H, N, inputs.sample_rows(B, H, N, per_head, 7000 + B))
+    check_rows(orc, q, k, v, scale, causal, o, lse, rows, "%s causal=%s" % (name, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_context_sampled(orc, causal):
+    q, k, v, meta = inputs.make_workload("long")
+    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+    scale = d ** -0.5
+    o, lse = run_gpu(q, k, v, scale, causal)
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    rows = inputs.sample_rows(B, H, N, inputs.LONG_ROWS_PER_HEAD, inputs.LONG_ROW_SAMPLE_SEED)
+    check_rows(orc, q, k, v, scale, causal, o, lse, rows, "long causal=%s" % causal)
