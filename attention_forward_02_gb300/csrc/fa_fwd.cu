@@ -28,11 +28,15 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 
+// Where P (the rounded softmax weights) lives between the two products.
+constexpr bool kPInTmem = true;
+
 template <int D, bool CAUSAL, typename T>
 cudaError_t set_smem_attr()
 {
-    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, T>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, fa::KCfg<D>::SMEM_ALLOC);
+    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, T, kPInTmem>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fa::KCfg<D, kPInTmem>::SMEM_ALLOC);
 }
 
 void init_device(int dev, DeviceState &st)
@@ -104,11 +108,13 @@ template <int D, bool CAUSAL, typename T>
 fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
                    float *lse, int BH, int N, float scale, cudaStream_t stream)
 {
-    const int num_q_tiles = (N + fa::kBM - 1) / fa::kBM;
+    const int num_q_blocks = (N + fa::kBM - 1) / fa::kBM;
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(num_q_tiles));
-    fa::fa_fwd_kernel<D, CAUSAL, T><<<grid, fa::kNumThreads, fa::KCfg<D>::SMEM_ALLOC, stream>>>(
-        mq, mk, mv, static_cast<T *>(o), lse, N, num_q_tiles, scale, scale_log2);
+    // one CTA per (Q block, batch*head), Q blocks of a head adjacent
+    const dim3 grid(static_cast<unsigned>(static_cast<long long>(BH) * num_q_blocks));
+    fa::fa_fwd_kernel<D, CAUSAL, T, kPInTmem>
+        <<<grid, fa::kNumThreads, fa::KCfg<D, kPInTmem>::SMEM_ALLOC, stream>>>(
+            mq, mk, mv, static_cast<T *>(o), lse, N, num_q_blocks, scale, scale_log2);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -141,8 +147,8 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
     const long long BH = static_cast<long long>(B) * H;
     if (BH > 0x7fffffffLL)
         return FA_ERR_UNSUPPORTED;
-    if ((N + fa::kBM - 1) / fa::kBM > 65535)
-        return FA_ERR_UNSUPPORTED;  // grid.y limit
+    if (BH * ((N + fa::kBM - 1) / fa::kBM) > 0x7fffffffLL)
+        return FA_ERR_UNSUPPORTED;  // grid.x limit
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 15u)
         return FA_ERR_MISALIGNED;

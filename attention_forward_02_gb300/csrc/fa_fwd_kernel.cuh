@@ -1,30 +1,36 @@
 // fa_fwd_kernel.cuh -- the sm_103a attention-forward kernel.
 //
-// What it computes: for one (batch*head, Q tile) per CTA,
-//   O_tile = softmax(Q_tile K^T * scale) V,  LSE_tile = m * scale + ln(l)
+// What it computes, for one (batch*head, 256-row Q block) per CTA:
+//   O = softmax(Q K^T * scale) V,   LSE = m * scale + ln(l)
 // with the online-softmax recurrence of "3.6 어텐션 I — 메모리 문제·
-// FlashAttention 원리", section 3.6.4 (state m, l, O kept on chip; alpha =
-// exp(m_old - m_new) rescales both l and O; one division by l at the end),
-// and the tile loop of section 3.6.6 (Q block fixed per CTA, K/V blocks
-// streamed; causal skips blocks above the diagonal and masks the diagonal).
-// The grid follows "Triton으로 FlashAttention 1·2 forward 구현하기", section
-// "병렬화 단위": one CTA per (Q block, batch*head).
+// FlashAttention 원리", section 3.6.4 (state m, l, O on chip; alpha rescales
+// both l and O; one division by l at the end) and the tile loop of section
+// 3.6.6 (Q block fixed per CTA, K/V blocks streamed; causal skips blocks above
+// the diagonal and masks the diagonal block).  The grid is FA2's: "Triton으로
+// FlashAttention 1·2 forward 구현하기", section "병렬화 단위" -- one CTA per
+// (Q block, batch*head); the Q blocks of one head are launched next to each
+// other so that their shared K/V stream stays in L2.
 //
-// GB300 mapping (differs from the pages' A100 cp.async / ldmatrix / mma.sync
-// design; see the design notes for the reasons):
-//   warp 4      : TMA producer.  Q tile once; K_j and V_j through a STAGES-deep
-//                 ring of 128B-swizzled shared-memory tiles (full/empty mbarriers).
-//   warp 5      : MMA issuer (one thread).  S_j = Q K_j^T into one of two TMEM
-//                 score buffers (tcgen05.mma, fp32 accumulate), then
-//                 O += P_{j-1} V_{j-1} into the TMEM output accumulator.
-//                 V is read as an MN-major B operand, so no transpose copy.
-//   warps 0..3  : softmax + correction + epilogue.  Thread t owns query row t
-//                 = TMEM lane t, so row max / row sum need no shuffles.  exp2
-//                 with scale*log2(e) folded into one FMA; P rounded to the input
-//                 dtype into a swizzled shared tile for the second MMA; O rescaled
-//                 in TMEM by alpha (skipped when the whole warp has alpha == 1);
-//                 epilogue O / l staged through shared memory and written with
-//                 coalesced 16-byte stores, LSE as one coalesced fp32 per row.
+// GB300 mapping (the pages' A100 design used cp.async, ldmatrix and mma.sync):
+//   The CTA's Q block is two 128-row sub-tiles h = 0, 1 (one M = 128 tcgen05
+//   MMA each) whose softmax work ping-pongs with the tensor core: while
+//   warpgroup h runs the softmax of tile j, the tensor core runs the other
+//   sub-tile's P V and Q K^T products.
+//   warp 9       TMA producer: Q0, Q1 once; then K_0, V_0, K_1, V_1, ... through
+//                a SLOTS-deep ring of 128B-swizzled shared tiles.
+//   warp 8       MMA issuer (one thread), per key tile j and sub-tile h:
+//                O_h += P_h,j V_j  then  S_h,j+1 = Q_h K_{j+1}^T  (tcgen05.mma,
+//                fp32 accumulators in TMEM).  V is an MN-major B operand.
+//   warps 4h..4h+3  softmax warpgroup of sub-tile h: thread t owns query row t
+//                = TMEM lane t.  It loads S, masks, takes the row max, updates
+//                the reference max, rescales l and O (in TMEM) by alpha, forms
+//                p = 2^(s*c - m*c) with one FMA + ex2, sums l in fp32, rounds P
+//                to the input dtype (into TMEM over S, or into shared memory),
+//                and finally writes O / l and LSE.
+// The reference max moves only when the row max grows by more than
+// kRescaleLog2 (in log2 units).  O and l always share the same reference, so
+// the final O / l and LSE are unchanged (the same algebra as section 3.6.4:
+// any common reference cancels in O / l); p stays <= 2^kRescaleLog2.
 // Every mbarrier wait is bounded: on expiry the CTA records a timeout in the
 // device status word, stops, waits (bounded) for its own copies and MMAs,
 // frees its TMEM and exits.
@@ -45,41 +51,57 @@ namespace fa {
 __device__ unsigned int g_fa_status;
 constexpr unsigned int kStatusTimeout = 1u;
 
-constexpr int kBM = 128;  // query rows per CTA: one M = 128 MMA, one TMEM lane per row
-constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kNumThreads = 192;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr uint32_t kTmemCols = 512;  // S0 @ 0, S1 @ 128, O @ 256
-constexpr uint32_t kTmemO = 256;
-constexpr long long kWaitLimitCycles = 1ll << 31;  // about one second at 2 GHz
-constexpr int kSwAtomBytes = 128 * 128;             // one [128 rows x 64 cols] 16-bit swizzle block
-
+constexpr int kSubM = 128;          // rows per sub-tile (one M = 128 MMA; one TMEM lane per row)
+constexpr int kBM = 2 * kSubM;      // query rows per CTA
+constexpr int kBN = 128;            // keys per K/V tile
+// Three warpgroups: two softmax warpgroups (warps 0-7) and a control
+// warpgroup (warp 8 MMA issuer, warp 9 TMA producer, warps 10-11 idle).
+// Launched at 168 registers per thread (384 x 168 = 64512); the control
+// warpgroup drops to 56 and the softmax warpgroups rise to 216:
+// 256 x 216 + 128 x 56 = 62464 <= 64512.
+constexpr int kNumThreads = 384;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 56;
+static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= 384 * 168, "register split");
+// TMEM columns: S0 @ 0, S1 @ 128, O0 @ 256, O1 @ 256 + D.  P_h (16-bit, two
+// per column) takes 64 columns: for D = 64 the spare columns 384 + 64 h, for
+// D = 128 the first half of S_h (the next S_h product is issued after the
+// P_h V product that reads it, and tcgen05.mma ops of one thread execute in
+// issue order).
+constexpr uint32_t kTmemCols = 512;
 template <int D>
+__host__ __device__ constexpr uint32_t tmem_p_col(int h)
+{
+    return D == 64 ? 384u + 64u * h : 128u * h;
+}
+constexpr float kRescaleLog2 = 8.0f;
+constexpr long long kWaitLimitCycles = 1ll << 31;  // about one second at 2 GHz
+constexpr int kSwAtomBytes = 128 * 128;             // [128 rows x 64 cols] 16-bit swizzle block
+
+template <int D, bool P_TMEM>
 struct KCfg {
-    static constexpr int STAGES = (D == 64) ? 3 : 2;
     static constexpr int TILE = 128 * D * 2;  // bytes of one [128, D] 16-bit tile
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + TILE;
-    static constexpr int V_OFF = K_OFF + STAGES * TILE;
-    static constexpr int P_OFF = V_OFF + STAGES * TILE;
-    static constexpr int P_BYTES = 128 * 128 * 2;
-    static constexpr int BAR_OFF = P_OFF + P_BYTES;
-    // barrier slots
+    static constexpr int SLOTS = P_TMEM ? (D == 64 ? 6 : 4) : (D == 64 ? 4 : 3);
+    static constexpr int Q_OFF = 0;           // Q0, Q1
+    static constexpr int KV_OFF = Q_OFF + 2 * TILE;
+    static constexpr int P_OFF = KV_OFF + SLOTS * TILE;  // P0, P1 (shared-memory variant)
+    static constexpr int P_TILE = 128 * kBN * 2;
+    static constexpr int BAR_OFF = P_OFF + (P_TMEM ? 0 : 2 * P_TILE);
     static constexpr int B_QFULL = 0;
-    static constexpr int B_KFULL = 1;
-    static constexpr int B_KEMPTY = B_KFULL + STAGES;
-    static constexpr int B_VFULL = B_KEMPTY + STAGES;
-    static constexpr int B_VEMPTY = B_VFULL + STAGES;
-    static constexpr int B_SFULL = B_VEMPTY + STAGES;  // two
-    static constexpr int B_PFULL = B_SFULL + 2;
-    static constexpr int B_ODONE = B_PFULL + 1;
-    static constexpr int B_DRAIN = B_ODONE + 1;
+    static constexpr int B_KVFULL = 1;
+    static constexpr int B_KVEMPTY = B_KVFULL + SLOTS;
+    static constexpr int B_SFULL = B_KVEMPTY + SLOTS;  // two
+    static constexpr int B_PFULL = B_SFULL + 2;        // two
+    static constexpr int B_OFINAL = B_PFULL + 2;       // two
+    static constexpr int B_DRAIN = B_OFINAL + 2;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // TMEM base address, abort flag
     static constexpr int SMEM_USED = SLOT_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * D <= static_cast<int>(kTmemCols), "TMEM budget");
 };
 
 template <typename T>
@@ -136,26 +158,27 @@ __device__ __forceinline__ void drain_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
-// Byte offset of 16-byte chunk `chunk` (0..D/8-1) of row `row` in a [128, D]
-// 16-bit tile laid out as D/64 column blocks of [128 rows x 128 B], each
-// 128B-swizzled (chunk index XOR row % 8) -- the layout TMA SWIZZLE_128B
-// writes and the tcgen05 SW128 descriptors read.
+// Byte offset of 16-byte chunk `chunk` of row `row` in a [128, 64*k] 16-bit
+// tile stored as k column blocks of [128 rows x 128 B], each 128B-swizzled
+// (chunk index XOR row % 8): the layout TMA SWIZZLE_128B writes and the
+// tcgen05 SW128 descriptors read.
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
 {
     return static_cast<uint32_t>((chunk >> 3) * kSwAtomBytes + row * 128 +
                                  (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-template <int D, bool CAUSAL, typename T>
+template <int D, bool CAUSAL, typename T, bool P_TMEM>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, T *__restrict__ out,
-                  float *__restrict__ lse, int N, int num_q_tiles, float scale, float scale_log2)
+                  float *__restrict__ lse, int N, int num_q_blocks, float scale, float scale_log2)
 {
-    using C = KCfg<D>;
-    constexpr int ST = C::STAGES;
-    constexpr int KSTEPS_QK = D / 16;   // UMMA_K = 16 for 16-bit operands
+    using C = KCfg<D, P_TMEM>;
+    constexpr int SLOTS = C::SLOTS;
+    constexpr int KSTEPS_QK = D / 16;  // UMMA_K = 16 for 16-bit operands
     constexpr int KSTEPS_PV = kBN / 16;
+    constexpr uint32_t kTmemO = 256;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -164,11 +187,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int q_tile = num_q_tiles - 1 - static_cast<int>(blockIdx.y);  // heavy causal tiles first
-    const int row0 = q_tile * kBM;
+    // Q blocks of one head are adjacent in launch order (shared K/V stays in
+    // L2); within a head the heaviest causal blocks go first.
+    const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(num_q_blocks));
+    const int qb = num_q_blocks - 1 - static_cast<int>(blockIdx.x % static_cast<unsigned>(num_q_blocks));
+    const int row0 = qb * kBM;
     const int num_k_tiles = (N + kBN - 1) / kBN;
-    const int nk = CAUSAL ? min(q_tile + 1, num_k_tiles) : num_k_tiles;
+    const int nk0 = CAUSAL ? min(2 * qb + 1, num_k_tiles) : num_k_tiles;  // sub-tile 0
+    const int nk1 = CAUSAL ? min(2 * qb + 2, num_k_tiles) : num_k_tiles;  // sub-tile 1 (>= nk0)
 
     auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + C::SLOT_OFF);
@@ -176,16 +202,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
-        for (int s = 0; s < ST; ++s) {
-            mbar_init(bar(C::B_KFULL + s), 1);
-            mbar_init(bar(C::B_KEMPTY + s), 1);
-            mbar_init(bar(C::B_VFULL + s), 1);
-            mbar_init(bar(C::B_VEMPTY + s), 1);
+        for (int s = 0; s < SLOTS; ++s) {
+            mbar_init(bar(C::B_KVFULL + s), 1);
+            mbar_init(bar(C::B_KVEMPTY + s), 1);
         }
-        mbar_init(bar(C::B_SFULL + 0), 1);
-        mbar_init(bar(C::B_SFULL + 1), 1);
-        mbar_init(bar(C::B_PFULL), 4 * 32);
-        mbar_init(bar(C::B_ODONE), 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(C::B_SFULL + h), 1);
+            mbar_init(bar(C::B_PFULL + h), 4 * 32);
+            mbar_init(bar(C::B_OFINAL + h), 1);
+        }
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -199,227 +224,269 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kTmaWarp) {
-        if (lane == 0) {
+    if (warp >= kMmaWarp) {
+      reg_dealloc<kRegsControl>();
+      if (warp == kTmaWarp && lane == 0) {
             // ---------------- producer ----------------
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
-            for (int b = 0; b < D / 64; ++b)
-                tma_load_3d(sbase + C::Q_OFF + b * kSwAtomBytes, &tm_q, bar(C::B_QFULL), b * 64, row0,
-                            bh, pol_q);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < nk; ++j) {
-                const int s = j % ST;
-                const uint32_t ph = (j / ST) & 1;
-                if (j >= ST && !wait_bounded(bar(C::B_KEMPTY + s), ph ^ 1, abort_flag))
-                    break;
-                mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE);
+            mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE);
+            for (int h = 0; h < 2; ++h)
                 for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(sbase + C::K_OFF + s * C::TILE + b * kSwAtomBytes, &tm_k,
-                                bar(C::B_KFULL + s), b * 64, j * kBN, bh, pol_kv);
-                ++k_issued;
-                if (j >= ST && !wait_bounded(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag))
+                    tma_load_3d(sbase + C::Q_OFF + h * C::TILE + b * kSwAtomBytes, &tm_q,
+                                bar(C::B_QFULL), b * 64, row0 + h * kSubM, bh, pol_q);
+            int issued = 0;  // loads into the ring: K_j = load 2j, V_j = load 2j + 1
+            for (int L = 0; L < 2 * nk1; ++L) {
+                const int s = L % SLOTS;
+                if (L >= SLOTS && !wait_bounded(bar(C::B_KVEMPTY + s), ((L / SLOTS) - 1) & 1, abort_flag))
                     break;
-                mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE);
+                const CUtensorMap *map = (L & 1) ? &tm_v : &tm_k;
+                mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE);
                 for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(sbase + C::V_OFF + s * C::TILE + b * kSwAtomBytes, &tm_v,
-                                bar(C::B_VFULL + s), b * 64, j * kBN, bh, pol_kv);
-                ++v_issued;
+                    tma_load_3d(sbase + C::KV_OFF + s * C::TILE + b * kSwAtomBytes, map,
+                                bar(C::B_KVFULL + s), b * 64, (L >> 1) * kBN, bh, pol_kv);
+                ++issued;
             }
             // Wait for every copy this thread issued (immediate on the normal
-            // path, where each one was consumed).  The last load into stage s
-            // was use number (issued - 1 - s) / ST of that stage.
+            // path, where each one was consumed).
             drain_bounded(bar(C::B_QFULL), 0);
-            for (int s = 0; s < ST; ++s) {
-                if (k_issued > s)
-                    drain_bounded(bar(C::B_KFULL + s), ((k_issued - 1 - s) / ST) & 1);
-                if (v_issued > s)
-                    drain_bounded(bar(C::B_VFULL + s), ((v_issued - 1 - s) / ST) & 1);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+            for (int s = 0; s < SLOTS; ++s)
+                if (issued > s)
+                    drain_bounded(bar(C::B_KVFULL + s), ((issued - 1 - s) / SLOTS) & 1);
+      } else if (warp == kMmaWarp && lane == 0) {
+        {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc_s = make_idesc_f16(DTypeTraits<T>::kBF16, kBM, kBN, false, false);
-            constexpr uint32_t idesc_o = make_idesc_f16(DTypeTraits<T>::kBF16, kBM, D, false, true);
-            bool ok = wait_bounded(bar(C::B_QFULL), 0, abort_flag);
-            tc_fence_after();
-            for (int j = 0; ok && j <= nk; ++j) {
-                if (j < nk) {
-                    const int s = j % ST;
-                    const uint32_t ph = (j / ST) & 1;
-                    ok = wait_bounded(bar(C::B_KFULL + s), ph, abort_flag);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    const uint32_t d_s = tmem + static_cast<uint32_t>(j & 1) * kBN;
-                    const uint32_t kt = sbase + C::K_OFF + s * C::TILE;
+            constexpr uint32_t idesc_s = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, kBN, false, false);
+            constexpr uint32_t idesc_o = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, D, false, true);
+            auto slot_of = [](int L) { return L % SLOTS; };
+            auto par_of = [](int L) { return static_cast<uint32_t>((L / SLOTS) & 1); };
+            auto issue_s = [&](int h, int j) {
+                const uint32_t kt = sbase + C::KV_OFF + slot_of(2 * j) * C::TILE;
+                const uint32_t qt = sbase + C::Q_OFF + h * C::TILE;
 #pragma unroll
-                    for (int kk = 0; kk < KSTEPS_QK; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
-                        const uint64_t ad = make_sdesc_sw128(sbase + C::Q_OFF + koff, 16, 1024);
-                        const uint64_t bd = make_sdesc_sw128(kt + koff, 16, 1024);
-                        umma_f16_ss(d_s, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(bar(C::B_SFULL + (j & 1)));
-                    umma_commit(bar(C::B_KEMPTY + s));
+                for (int kk = 0; kk < KSTEPS_QK; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
+                    umma_f16_ss(tmem + h * kBN, make_sdesc_sw128(qt + koff, 16, 1024),
+                                make_sdesc_sw128(kt + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 }
-                if (j >= 1) {
-                    const int i = j - 1;
-                    const int s = i % ST;
-                    const uint32_t ph = (i / ST) & 1;
-                    ok = wait_bounded(bar(C::B_PFULL), i & 1, abort_flag);
-                    if (!ok)
-                        break;
-                    ok = wait_bounded(bar(C::B_VFULL + s), ph, abort_flag);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    const uint32_t vt = sbase + C::V_OFF + s * C::TILE;
+            };
+            auto issue_pv = [&](int h, int j) {
+                const uint32_t vt = sbase + C::KV_OFF + slot_of(2 * j + 1) * C::TILE;
+                const uint32_t od = tmem + kTmemO + h * D;
 #pragma unroll
-                    for (int kk = 0; kk < KSTEPS_PV; ++kk) {
+                for (int kk = 0; kk < KSTEPS_PV; ++kk) {
+                    // V: MN-major; 16 key rows (2048 B) per K step; the two
+                    // 64-column blocks of D = 128 are kSwAtomBytes apart.
+                    const uint64_t bd = make_sdesc_sw128(vt + kk * 2048, kSwAtomBytes, 1024);
+                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                    if constexpr (P_TMEM) {
+                        // P_h,j: 16-bit, packed two per column; 8 columns per K step
+                        umma_f16_ts(od, tmem + tmem_p_col<D>(h) + kk * 8, bd, idesc_o, acc);
+                    } else {
+                        const uint32_t pt = sbase + C::P_OFF + h * C::P_TILE;
                         const uint32_t poff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
-                        const uint64_t ad = make_sdesc_sw128(sbase + C::P_OFF + poff, 16, 1024);
-                        // V tile: MN-major; 16 key rows (2048 B) per K step, the
-                        // two 64-column blocks of d = 128 are kSwAtomBytes apart.
-                        const uint64_t bd = make_sdesc_sw128(vt + kk * 2048, kSwAtomBytes, 1024);
-                        umma_f16_ss(tmem + kTmemO, ad, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                        umma_f16_ss(od, make_sdesc_sw128(pt + poff, 16, 1024), bd, idesc_o, acc);
                     }
-                    umma_commit(bar(C::B_ODONE));
-                    umma_commit(bar(C::B_VEMPTY + s));
                 }
+            };
+            bool ok = wait_bounded(bar(C::B_QFULL), 0, abort_flag) &&
+                      wait_bounded(bar(C::B_KVFULL + slot_of(0)), par_of(0), abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                umma_commit(bar(C::B_SFULL + 0));
+                issue_s(1, 0);
+                umma_commit(bar(C::B_SFULL + 1));
+                umma_commit(bar(C::B_KVEMPTY + slot_of(0)));
+            }
+            for (int j = 0; ok && j < nk1; ++j) {
+                ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 1)), par_of(2 * j + 1), abort_flag);
+                bool have_next_k = false;
+                for (int h = 0; ok && h < 2; ++h) {
+                    const int nkh = h == 0 ? nk0 : nk1;
+                    if (j >= nkh)
+                        continue;
+                    ok = wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    issue_pv(h, j);
+                    if (j + 1 < nkh) {
+                        if (!have_next_k) {
+                            ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 2)), par_of(2 * j + 2),
+                                              abort_flag);
+                            if (!ok)
+                                break;
+                            tc_fence_after();
+                            have_next_k = true;
+                        }
+                        issue_s(h, j + 1);
+                        umma_commit(bar(C::B_SFULL + h));
+                    } else {
+                        umma_commit(bar(C::B_OFINAL + h));
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 1)));  // V_j: both P V products issued
+                if (have_next_k)
+                    umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 2)));  // K_{j+1}: both S products
             }
             // every MMA issued above has completed once this arrives
             umma_commit(bar(C::B_DRAIN));
             drain_bounded(bar(C::B_DRAIN), 0);
         }
+      }
     } else {
-        // ---------------- softmax / correction / epilogue (warps 0..3) ----------------
-        const int r = threadIdx.x;  // row within the tile == TMEM lane
-        const int qrow = row0 + r;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        float m = -INFINITY;  // running max of raw scores (scale >= 0)
+        reg_alloc<kRegsSoftmax>();
+        // ---------------- softmax warpgroup h (warps 4h .. 4h+3) ----------------
+        const int h = warp >> 2;
+        const int r = threadIdx.x & 127;  // row within the sub-tile == TMEM lane
+        const int qrow = row0 + h * kSubM + r;
+        const int nkh = h == 0 ? nk0 : nk1;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(h * kBN);
+        const uint32_t o_tm = tmem + lane_base + kTmemO + static_cast<uint32_t>(h * D);
+        const uint32_t p_tm = tmem + lane_base + tmem_p_col<D>(h);
+        float m_ref = -INFINITY;  // reference max (raw score units; scale >= 0)
         float l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nk; ++j) {
-            ok = wait_bounded(bar(C::B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag);
+        for (int j = 0; j < nkh; ++j) {
+            ok = wait_bounded(bar(C::B_SFULL + h), j & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
             tc_fence_after();
-            float p[kBN];
+            float s[kBN];
             {
                 uint32_t u[32];
 #pragma unroll
                 for (int c4 = 0; c4 < kBN / 32; ++c4) {
-                    tmem_ld32(tmem + lane_base + static_cast<uint32_t>(j & 1) * kBN + c4 * 32, u);
+                    tmem_ld32(s_tm + c4 * 32, u);
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                        p[c4 * 32 + c] = __uint_as_float(u[c]);
+                        s[c4 * 32 + c] = __uint_as_float(u[c]);
                 }
             }
+            // keys [kbase, kbase + limit) are allowed for this row (limit >= 1)
             const int kbase = j * kBN;
-            int limit = kBN;  // keys [kbase, kbase + limit) are allowed for this row
-            if (kbase + kBN > N)
-                limit = N - kbase;
-            if (CAUSAL && j == nk - 1)
+            int limit = min(kBN, N - kbase);
+            if (CAUSAL)
                 limit = min(limit, qrow - kbase + 1);
             const bool masked = __any_sync(0xffffffffu, limit < kBN);
             if (masked) {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c)
                     if (c >= limit)
-                        p[c] = -INFINITY;
+                        s[c] = -INFINITY;
             }
-            float mt = p[0];
+            float mx[8];
 #pragma unroll
-            for (int c = 1; c < kBN; ++c)
-                mt = fmaxf(mt, p[c]);
-            const float m_new = fmaxf(m, mt);
-            // alpha = exp(m_old - m_new); 0 while no score has been seen (m = -inf),
-            // which also covers scale == 0 where (-inf) * 0 would be NaN.
-            const float alpha = (m == -INFINITY) ? 0.f : ex2_approx((m - m_new) * scale_log2);
-            const float neg_mc = (m_new == -INFINITY) ? 0.f : -m_new * scale_log2;
-            float rsum = 0.f;
+            for (int i = 0; i < 8; ++i)
+                mx[i] = s[i];
+#pragma unroll
+            for (int c = 8; c < kBN; ++c)
+                mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            // Move the reference max only when the row max grows by more than
+            // kRescaleLog2 (log2 units); the first tile always sets it.
+            float alpha = 1.f;
+            if (m_ref == -INFINITY) {
+                alpha = 0.f;
+                m_ref = mt;
+            } else if ((mt - m_ref) * scale_log2 > kRescaleLog2) {
+                alpha = ex2_approx((m_ref - mt) * scale_log2);
+                m_ref = mt;
+            }
+            l *= alpha;
+            const float neg_mc = -m_ref * scale_log2;
+            float sm[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                sm[i] = 0.f;
             if (masked) {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) {
-                    const float e = (c < limit) ? ex2_approx(fmaf(p[c], scale_log2, neg_mc)) : 0.f;
-                    p[c] = e;
-                    rsum += e;
+                    const float e = (c < limit) ? ex2_approx(fmaf(s[c], scale_log2, neg_mc)) : 0.f;
+                    s[c] = e;
+                    sm[c & 7] += e;
                 }
             } else {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) {
-                    const float e = ex2_approx(fmaf(p[c], scale_log2, neg_mc));
-                    p[c] = e;
-                    rsum += e;
+                    const float e = ex2_approx(fmaf(s[c], scale_log2, neg_mc));
+                    s[c] = e;
+                    sm[c & 7] += e;
                 }
             }
-            l = l * alpha + rsum;
-            m = m_new;
+            l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
 
-            if (j > 0) {
-                // PV_{j-1} must be complete: it read the P buffer and wrote O.
-                ok = wait_bounded(bar(C::B_ODONE), (j - 1) & 1, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            // P_h,j rounded to the input dtype
+            if constexpr (P_TMEM) {
 #pragma unroll
-                    for (int c4 = 0; c4 < D / 32; ++c4) {
-                        uint32_t u[32];
-                        const uint32_t ta = tmem + lane_base + kTmemO + c4 * 32;
-                        tmem_ld32(ta, u);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t w[32];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            u[c] = __float_as_uint(__uint_as_float(u[c]) * alpha);
-                        tmem_st32(ta, u);
-                    }
-                    tmem_wait_st();
+                    for (int c = 0; c < 32; ++c)
+                        w[c] = DTypeTraits<T>::pack(s[half * 64 + 2 * c], s[half * 64 + 2 * c + 1]);
+                    tmem_st32(p_tm + half * 32, w);
+                }
+            } else {
+                const uint32_t pt = sbase + C::P_OFF + h * C::P_TILE;
+#pragma unroll
+                for (int ch = 0; ch < kBN / 8; ++ch) {
+                    const uint32_t w0 = DTypeTraits<T>::pack(s[ch * 8 + 0], s[ch * 8 + 1]);
+                    const uint32_t w1 = DTypeTraits<T>::pack(s[ch * 8 + 2], s[ch * 8 + 3]);
+                    const uint32_t w2 = DTypeTraits<T>::pack(s[ch * 8 + 4], s[ch * 8 + 5]);
+                    const uint32_t w3 = DTypeTraits<T>::pack(s[ch * 8 + 6], s[ch * 8 + 7]);
+                    st_shared_v4(pt + sw128_offset(r, ch), w0, w1, w2, w3);
+                }
+                fence_proxy_async_smem();
+            }
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // O_h holds P V up to tile j-1 (the S_h,j product, issued after
+                // P_h,j-1 V_{j-1}, has completed) and P_h,j V_j is not issued
+                // before this warpgroup arrives below.
+#pragma unroll
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    uint32_t u[32];
+                    tmem_ld32(o_tm + c4 * 32, u);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        u[c] = __float_as_uint(__uint_as_float(u[c]) * alpha);
+                    tmem_st32(o_tm + c4 * 32, u);
                 }
             }
-            // P_j (rounded to the input dtype) into the swizzled K-major tile.
-            const uint32_t prow = sbase + C::P_OFF;
-#pragma unroll
-            for (int ch = 0; ch < kBN / 8; ++ch) {
-                const uint32_t w0 = DTypeTraits<T>::pack(p[ch * 8 + 0], p[ch * 8 + 1]);
-                const uint32_t w1 = DTypeTraits<T>::pack(p[ch * 8 + 2], p[ch * 8 + 3]);
-                const uint32_t w2 = DTypeTraits<T>::pack(p[ch * 8 + 4], p[ch * 8 + 5]);
-                const uint32_t w3 = DTypeTraits<T>::pack(p[ch * 8 + 6], p[ch * 8 + 7]);
-                st_shared_v4(prow + sw128_offset(r, ch), w0, w1, w2, w3);
-            }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
+            mbar_arrive(bar(C::B_PFULL + h));
         }
 
-        // ---------------- epilogue ----------------
-        // Every softmax thread reaches the named barrier below, whatever
-        // happened; a warp that gave up has set the abort flag first, so after
-        // the barrier all four warps agree on whether the staged tile is whole.
+        // ---------------- epilogue of sub-tile h ----------------
+        // Every thread of the warpgroup reaches the named barrier; a warp that
+        // gave up has set the abort flag first, so after the barrier the four
+        // warps agree on whether the staged tile is whole.
         if (ok) {
-            ok = wait_bounded(bar(C::B_ODONE), (nk - 1) & 1, abort_flag);
+            ok = wait_bounded(bar(C::B_OFINAL + h), 0, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
-        const uint32_t stage = sbase + C::Q_OFF;  // Q tile is dead: every S MMA completed
+        // Q_h is dead: every product that read it has completed.
+        const uint32_t stage = sbase + C::Q_OFF + h * C::TILE;
         if (ok) {
             tc_fence_after();
             const float inv_l = 1.f / l;
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 uint32_t u[32];
-                tmem_ld32(tmem + lane_base + kTmemO + c4 * 32, u);
+                tmem_ld32(o_tm + c4 * 32, u);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const int ch = c4 * 4 + q4;
                     const float *f = reinterpret_cast<const float *>(u) + q4 * 8;
-                    st_shared_v4(stage + sw128_offset(r, ch),
+                    st_shared_v4(stage + sw128_offset(r, c4 * 4 + q4),
                                  DTypeTraits<T>::pack(f[0] * inv_l, f[1] * inv_l),
                                  DTypeTraits<T>::pack(f[2] * inv_l, f[3] * inv_l),
                                  DTypeTraits<T>::pack(f[4] * inv_l, f[5] * inv_l),
@@ -427,19 +494,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             }
             if (lse != nullptr && qrow < N)
-                lse[static_cast<size_t>(bh) * N + qrow] = m * scale + logf(l);
+                lse[static_cast<size_t>(bh) * N + qrow] = m_ref * scale + logf(l);
         }
-        named_bar_sync(1, 4 * 32);
+        named_bar_sync(1 + h, 4 * 32);
         if (*abort_flag == 0) {
             constexpr int CHUNKS_PER_ROW = D / 8;
+            const int srow0 = row0 + h * kSubM;
             uint8_t *obase = reinterpret_cast<uint8_t *>(out) +
-                             (static_cast<size_t>(bh) * N + row0) * D * sizeof(T);
+                             (static_cast<size_t>(bh) * N + srow0) * D * sizeof(T);
 #pragma unroll 4
-            for (int idx = r; idx < kBM * CHUNKS_PER_ROW; idx += 4 * 32) {
+            for (int idx = r; idx < kSubM * CHUNKS_PER_ROW; idx += 4 * 32) {
                 const int row = idx / CHUNKS_PER_ROW;
                 const int ch = idx % CHUNKS_PER_ROW;
                 const uint4 val = ld_shared_v4(stage + sw128_offset(row, ch));
-                if (row0 + row < N)
+                if (srow0 + row < N)
                     *reinterpret_cast<uint4 *>(obase + (static_cast<size_t>(row) * D + ch * 8) *
                                                            sizeof(T)) = val;
             }

@@ -67,7 +67,7 @@ def call(q=Q, k=K, v=V, o=O, lse=L, B=1, H=2, N=256, d=64, scale=0.125, causal=0
     (dict(q=Q + 2), 3), (dict(k=K + 8), 3), (dict(o=O + 4), 3), (dict(lse=L + 2), 3),
     (dict(o=Q + 4096), 1),          # output overlaps q
     (dict(lse=O + 64), 1),          # lse overlaps o
-    (dict(N=65535 * 128 + 1), 2),   # more Q tiles than the grid allows
+    (dict(B=65536, H=65536), 2),    # more CTAs than a 1-D grid allows
     (dict(N=0), 0), (dict(B=0), 0), (dict(H=0, q=0, o=0), 0),  # empty problems
 ], ids=lambda x: str(x))
 def test_argument_checks(lib, kwargs, status):
