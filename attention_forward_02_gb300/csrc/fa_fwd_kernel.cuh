@@ -57,13 +57,13 @@ constexpr int kBN = 128;            // keys per K/V tile
 // Three warpgroups: two softmax warpgroups (warps 0-7) and a control
 // warpgroup (warp 8 MMA issuer, warp 9 TMA producer, warps 10-11 idle).
 // Launched at 168 registers per thread (384 x 168 = 64512); the control
-// warpgroup drops to 56 and the softmax warpgroups rise to 216:
-// 256 x 216 + 128 x 56 = 62464 <= 64512.
+// warpgroup drops to 80 and the softmax warpgroups rise to 208:
+// 256 x 208 + 128 x 80 = 63488 <= 64512.
 constexpr int kNumThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsControl = 56;
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsControl = 80;
 static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= 384 * 168, "register split");
 // TMEM columns: S0 @ 0, S1 @ 128, O0 @ 256, O1 @ 256 + D.  P_h (16-bit, two
 // per column) takes 64 columns: for D = 64 the spare columns 384 + 64 h, for
@@ -166,6 +166,58 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
 {
     return static_cast<uint32_t>((chunk >> 3) * kSwAtomBytes + row * 128 +
                                  (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// Masks keys c >= limit of one row of scores (set to -inf).
+__device__ __forceinline__ void mask_tail(float (&s)[kBN], int limit)
+{
+#pragma unroll
+    for (int c = 0; c < kBN; ++c)
+        if (c >= limit)
+            s[c] = -INFINITY;
+}
+
+// Row maximum of 128 scores: eight independent three-input max chains.
+__device__ __forceinline__ float row_max(const float (&s)[kBN])
+{
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        a[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+    for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            a[i] = fmax3(a[i], s[c + 2 * i], s[c + 2 * i + 1]);
+    return fmaxf(fmax3(a[0], a[1], a[2]), fmax3(fmax3(a[3], a[4], a[5]), a[6], a[7]));
+}
+
+// In place: s[c] <- 2^(s[c] * c2 + neg_mc) (0 for masked keys c >= limit);
+// returns the row sum, accumulated as four packed pairs.
+template <bool MASKED>
+__device__ __forceinline__ float exp_tile(float (&s)[kBN], int limit, float c2, float neg_mc)
+{
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        acc[i] = make_float2(0.f, 0.f);
+    const float2 cc = make_float2(c2, c2);
+    const float2 nn = make_float2(neg_mc, neg_mc);
+#pragma unroll
+    for (int c = 0; c < kBN; c += 2) {
+        const float2 x = ffma2(make_float2(s[c], s[c + 1]), cc, nn);
+        float e0 = ex2_approx(x.x);
+        float e1 = ex2_approx(x.y);
+        if (MASKED) {
+            e0 = (c < limit) ? e0 : 0.f;
+            e1 = (c + 1 < limit) ? e1 : 0.f;
+        }
+        s[c] = e0;
+        s[c + 1] = e1;
+        acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], make_float2(e0, e1));
+    }
+    const float2 t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    return t.x + t.y;
 }
 
 template <int D, bool CAUSAL, typename T, bool P_TMEM>
@@ -361,80 +413,53 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 break;
             tc_fence_after();
             float s[kBN];
-            {
-                uint32_t u[32];
-#pragma unroll
-                for (int c4 = 0; c4 < kBN / 32; ++c4) {
-                    tmem_ld32(s_tm + c4 * 32, u);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        s[c4 * 32 + c] = __uint_as_float(u[c]);
-                }
-            }
+            tmem_ld128(s_tm, s);
             // keys [kbase, kbase + limit) are allowed for this row (limit >= 1)
             const int kbase = j * kBN;
             int limit = min(kBN, N - kbase);
             if (CAUSAL)
                 limit = min(limit, qrow - kbase + 1);
             const bool masked = __any_sync(0xffffffffu, limit < kBN);
-            if (masked) {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    if (c >= limit)
-                        s[c] = -INFINITY;
-            }
-            float mx[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                mx[i] = s[i];
-#pragma unroll
-            for (int c = 8; c < kBN; ++c)
-                mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            // Move the reference max only when the row max grows by more than
-            // kRescaleLog2 (log2 units); the first tile always sets it.
+            if (masked)
+                mask_tail(s, limit);
+            // Tile 0 sets the reference max from its own row max.  Later tiles
+            // exponentiate against the current reference while their row max
+            // is taken; only a row max that outgrows the reference by more than
+            // kRescaleLog2 (rare) sends the warp down the redo path.
             float alpha = 1.f;
-            if (m_ref == -INFINITY) {
+            float rsum;
+            if (j == 0) {
+                m_ref = row_max(s);
                 alpha = 0.f;
-                m_ref = mt;
-            } else if ((mt - m_ref) * scale_log2 > kRescaleLog2) {
-                alpha = ex2_approx((m_ref - mt) * scale_log2);
-                m_ref = mt;
-            }
-            l *= alpha;
-            const float neg_mc = -m_ref * scale_log2;
-            float sm[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                sm[i] = 0.f;
-            if (masked) {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const float e = (c < limit) ? ex2_approx(fmaf(s[c], scale_log2, neg_mc)) : 0.f;
-                    s[c] = e;
-                    sm[c & 7] += e;
-                }
+                rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                              : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
             } else {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const float e = ex2_approx(fmaf(s[c], scale_log2, neg_mc));
-                    s[c] = e;
-                    sm[c & 7] += e;
+                const float mt = row_max(s);
+                rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                              : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
+                const bool grow = (mt - m_ref) * scale_log2 > kRescaleLog2;
+                if (__any_sync(0xffffffffu, grow)) {
+                    if (grow) {
+                        alpha = ex2_approx((m_ref - mt) * scale_log2);
+                        m_ref = mt;
+                    }
+                    // S_h is intact until P_h is written below: redo the tile
+                    tmem_ld128(s_tm, s);
+                    if (masked)
+                        mask_tail(s, limit);
+                    rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                                  : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
                 }
             }
-            l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+            l = l * alpha + rsum;
 
             // P_h,j rounded to the input dtype
             if constexpr (P_TMEM) {
+                uint32_t w[64];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        w[c] = DTypeTraits<T>::pack(s[half * 64 + 2 * c], s[half * 64 + 2 * c + 1]);
-                    tmem_st32(p_tm + half * 32, w);
-                }
+                for (int c = 0; c < 64; ++c)
+                    w[c] = DTypeTraits<T>::pack(s[2 * c], s[2 * c + 1]);
+                tmem_st64(p_tm, w);
             } else {
                 const uint32_t pt = sbase + C::P_OFF + h * C::P_TILE;
 #pragma unroll
@@ -456,8 +481,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     uint32_t u[32];
                     tmem_ld32(o_tm + c4 * 32, u);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        u[c] = __float_as_uint(__uint_as_float(u[c]) * alpha);
+                    for (int c = 0; c < 32; c += 2) {
+                        const float2 v = fmul2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
+                                               make_float2(alpha, alpha));
+                        u[c] = __float_as_uint(v.x);
+                        u[c + 1] = __float_as_uint(v.y);
+                    }
                     tmem_st32(o_tm + c4 * 32, u);
                 }
             }
