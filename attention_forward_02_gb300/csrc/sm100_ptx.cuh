@@ -234,6 +234,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "memory");
 }
 
+// 64 consecutive columns: two .x32 loads, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&f)[64])
+{
+    uint32_t(&r)[64] = reinterpret_cast<uint32_t(&)[64]>(f);
+    asm volatile(
+        "{\n\t.reg .b32 t;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "add.u32 t, %64, 32;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [t];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t}"
+        : FA_R32(r), FA_R32((r + 32))
+        : "r"(taddr)
+        : "memory");
+}
+
 // 128 consecutive columns: four .x32 loads, one wait.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&f)[128])
 {
