@@ -28,11 +28,15 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 
+// Where P (the rounded softmax weights) lives between the two products.
+constexpr bool kPInTmem = true;
+
 template <int D, bool CAUSAL, typename T>
 cudaError_t set_smem_attr()
 {
-    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, T>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, fa::KCfg<D>::SMEM_ALLOC);
+    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, T, kPInTmem>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fa::KCfg<D, kPInTmem>::SMEM_ALLOC);
 }
 
 void init_device(int dev, DeviceState &st)
@@ -108,7 +112,8 @@ fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     // one CTA per (Q block, batch*head), Q blocks of a head adjacent
     const dim3 grid(static_cast<unsigned>(static_cast<long long>(BH) * num_q_blocks));
-    fa::fa_fwd_kernel<D, CAUSAL, T><<<grid, fa::kNumThreads, fa::KCfg<D>::SMEM_ALLOC, stream>>>(
+    fa::fa_fwd_kernel<D, CAUSAL, T, kPInTmem>
+        <<<grid, fa::kNumThreads, fa::KCfg<D, kPInTmem>::SMEM_ALLOC, stream>>>(
             mq, mk, mv, static_cast<T *>(o), lse, N, num_q_blocks, scale, scale_log2);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

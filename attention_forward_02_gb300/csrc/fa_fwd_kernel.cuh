@@ -14,28 +14,23 @@
 // GB300 mapping (the pages' A100 design used cp.async, ldmatrix and mma.sync):
 //   The CTA's Q block is two 128-row sub-tiles h = 0, 1 (one M = 128 tcgen05
 //   MMA each) whose softmax work ping-pongs with the tensor core: while
-//   sub-tile h runs the softmax of key tile j, the tensor core runs the other
+//   warpgroup h runs the softmax of tile j, the tensor core runs the other
 //   sub-tile's P V and Q K^T products.
-//   warp 17      TMA producer: Q0, Q1 once; then K_0, V_0, K_1, V_1, ... through
+//   warp 9       TMA producer: Q0, Q1 once; then K_0, V_0, K_1, V_1, ... through
 //                a SLOTS-deep ring of 128B-swizzled shared tiles.
-//   warp 16      MMA issuer (one thread), per key tile j and sub-tile h:
+//   warp 8       MMA issuer (one thread), per key tile j and sub-tile h:
 //                O_h += P_h,j V_j  then  S_h,j+1 = Q_h K_{j+1}^T  (tcgen05.mma,
 //                fp32 accumulators in TMEM).  V is an MN-major B operand.
-//   warps 0-15   softmax: sub-tile h = warp / 8 uses warps 8h .. 8h+7.  Query
-//                row r of the sub-tile is TMEM lane r; its 128 scores are split
-//                between two threads -- half a = 0 takes keys 0-63 (warp
-//                8h + r/32), half a = 1 keys 64-127 (warp 8h + 4 + r/32).  The
-//                two halves run on the same SM sub-partition and hide each
-//                other's latency; they exchange partial row maxima (and, at the
-//                end, partial sums) through shared memory.
-// Per key tile each thread loads its 64 scores, masks, takes the partial row
-// max, exponentiates p = 2^(s*c - m*c) (one packed FMA per pair + ex2) against
-// the current reference max, sums, and writes P (rounded to the input dtype)
-// into TMEM for the second product.  The reference max moves only when the row
-// max grows by more than kRescaleLog2 (log2 units), which is rare; then the
-// tile is redone against the new max and l and O are rescaled by alpha.  O and
-// l always share the same reference, so O / l and LSE are unchanged (any
-// common reference cancels, the algebra of section 3.6.4); p <= 2^kRescaleLog2.
+//   warps 4h..4h+3  softmax warpgroup of sub-tile h: thread t owns query row t
+//                = TMEM lane t.  It loads S, masks, takes the row max, updates
+//                the reference max, rescales l and O (in TMEM) by alpha, forms
+//                p = 2^(s*c - m*c) with one FMA + ex2, sums l in fp32, rounds P
+//                to the input dtype (into TMEM over S, or into shared memory),
+//                and finally writes O / l and LSE.
+// The reference max moves only when the row max grows by more than
+// kRescaleLog2 (in log2 units).  O and l always share the same reference, so
+// the final O / l and LSE are unchanged (the same algebra as section 3.6.4:
+// any common reference cancels in O / l); p stays <= 2^kRescaleLog2.
 // Every mbarrier wait is bounded: on expiry the CTA records a timeout in the
 // device status word, stops, waits (bounded) for its own copies and MMAs,
 // frees its TMEM and exits.
@@ -56,23 +51,20 @@ namespace fa {
 __device__ unsigned int g_fa_status;
 constexpr unsigned int kStatusTimeout = 1u;
 
-constexpr int kSubM = 128;       // rows per sub-tile (one M = 128 MMA; one TMEM lane per row)
-constexpr int kBM = 2 * kSubM;   // query rows per CTA
-constexpr int kBN = 128;         // keys per K/V tile
-constexpr int kHalf = kBN / 2;   // keys per softmax thread
-// Five warpgroups: four softmax warpgroups (warps 0-15) and a control
-// warpgroup (warp 16 MMA issuer, warp 17 TMA producer, warps 18-19 idle).
-// Launched at 96 registers per thread (640 x 96 = 61440); the control
-// warpgroup drops to kRegsControl and the softmax warps rise to kRegsSoftmax.
-constexpr int kNumThreads = 640;
-constexpr int kNumSoftmaxThreads = 512;
-constexpr int kMmaWarp = 16;
-constexpr int kTmaWarp = 17;
-constexpr uint32_t kLaunchRegs = 96;
-constexpr uint32_t kRegsSoftmax = 104;
-constexpr uint32_t kRegsControl = 64;
-static_assert(kNumSoftmaxThreads * kRegsSoftmax + 128 * kRegsControl <= kNumThreads * kLaunchRegs,
-              "register split");
+constexpr int kSubM = 128;          // rows per sub-tile (one M = 128 MMA; one TMEM lane per row)
+constexpr int kBM = 2 * kSubM;      // query rows per CTA
+constexpr int kBN = 128;            // keys per K/V tile
+// Three warpgroups: two softmax warpgroups (warps 0-7) and a control
+// warpgroup (warp 8 MMA issuer, warp 9 TMA producer, warps 10-11 idle).
+// Launched at 168 registers per thread (384 x 168 = 64512); the control
+// warpgroup drops to 80 and the softmax warpgroups rise to 208:
+// 256 x 208 + 128 x 80 = 63488 <= 64512.
+constexpr int kNumThreads = 384;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsControl = 80;
+static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= 384 * 168, "register split");
 // TMEM columns: S0 @ 0, S1 @ 128, O0 @ 256, O1 @ 256 + D.  P_h (16-bit, two
 // per column) takes 64 columns: for D = 64 the spare columns 384 + 64 h, for
 // D = 128 the first half of S_h (the next S_h product is issued after the
@@ -88,22 +80,24 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitLimitCycles = 1ll << 31;  // about one second at 2 GHz
 constexpr int kSwAtomBytes = 128 * 128;             // [128 rows x 64 cols] 16-bit swizzle block
 
-template <int D>
+template <int D, bool P_TMEM>
 struct KCfg {
     static constexpr int TILE = 128 * D * 2;  // bytes of one [128, D] 16-bit tile
-    static constexpr int SLOTS = D == 64 ? 6 : 4;
-    static constexpr int Q_OFF = 0;           // Q0, Q1 (later the O staging of each sub-tile)
+    static constexpr int SLOTS = P_TMEM ? (D == 64 ? 6 : 4) : (D == 64 ? 4 : 3);
+    static constexpr int Q_OFF = 0;           // Q0, Q1
     static constexpr int KV_OFF = Q_OFF + 2 * TILE;
-    static constexpr int X_OFF = KV_OFF + SLOTS * TILE;  // float [2 parity][2 h][2 half][128 rows]
-    static constexpr int X_BYTES = 2 * 2 * 2 * 128 * 4;
-    static constexpr int BAR_OFF = X_OFF + X_BYTES;
+    static constexpr int P_OFF = KV_OFF + SLOTS * TILE;  // P0, P1 (shared-memory variant)
+    static constexpr int P_TILE = 128 * kBN * 2;
+    static constexpr int BAR_OFF = P_OFF + (P_TMEM ? 0 : 2 * P_TILE);
     static constexpr int B_QFULL = 0;
     static constexpr int B_KVFULL = 1;
     static constexpr int B_KVEMPTY = B_KVFULL + SLOTS;
     static constexpr int B_SFULL = B_KVEMPTY + SLOTS;  // two
     static constexpr int B_PFULL = B_SFULL + 2;        // two
     static constexpr int B_OFINAL = B_PFULL + 2;       // two
-    static constexpr int B_DRAIN = B_OFINAL + 2;
+    static constexpr int B_SFREE = B_OFINAL + 2;       // two (early-S order only)
+    static constexpr int B_OREADY = B_SFREE + 2;       // two (early-S order only)
+    static constexpr int B_DRAIN = B_OREADY + 2;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // TMEM base address, abort flag
     static constexpr int SMEM_USED = SLOT_OFF + 16;
@@ -176,24 +170,24 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
                                  (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// Masks keys c >= limit of one half-row of scores (set to -inf).
-__device__ __forceinline__ void mask_tail(float (&s)[kHalf], int limit)
+// Masks keys c >= limit of one row of scores (set to -inf).
+__device__ __forceinline__ void mask_tail(float (&s)[kBN], int limit)
 {
 #pragma unroll
-    for (int c = 0; c < kHalf; ++c)
+    for (int c = 0; c < kBN; ++c)
         if (c >= limit)
             s[c] = -INFINITY;
 }
 
-// Maximum of 64 scores: eight independent three-input max chains.
-__device__ __forceinline__ float half_max(const float (&s)[kHalf])
+// Row maximum of 128 scores: eight independent three-input max chains.
+__device__ __forceinline__ float row_max(const float (&s)[kBN])
 {
     float a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         a[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-    for (int c = 16; c < kHalf; c += 16)
+    for (int c = 16; c < kBN; c += 16)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             a[i] = fmax3(a[i], s[c + 2 * i], s[c + 2 * i + 1]);
@@ -201,9 +195,9 @@ __device__ __forceinline__ float half_max(const float (&s)[kHalf])
 }
 
 // In place: s[c] <- 2^(s[c] * c2 + neg_mc) (0 for masked keys c >= limit);
-// returns the sum, accumulated as four packed pairs.
+// returns the row sum, accumulated as four packed pairs.
 template <bool MASKED>
-__device__ __forceinline__ float exp_half(float (&s)[kHalf], int limit, float c2, float neg_mc)
+__device__ __forceinline__ float exp_tile(float (&s)[kBN], int limit, float c2, float neg_mc)
 {
     float2 acc[4];
 #pragma unroll
@@ -212,7 +206,7 @@ __device__ __forceinline__ float exp_half(float (&s)[kHalf], int limit, float c2
     const float2 cc = make_float2(c2, c2);
     const float2 nn = make_float2(neg_mc, neg_mc);
 #pragma unroll
-    for (int c = 0; c < kHalf; c += 2) {
+    for (int c = 0; c < kBN; c += 2) {
         const float2 x = ffma2(make_float2(s[c], s[c + 1]), cc, nn);
         float e0 = ex2_approx(x.x);
         float e1 = ex2_approx(x.y);
@@ -228,13 +222,18 @@ __device__ __forceinline__ float exp_half(float (&s)[kHalf], int limit, float c2
     return t.x + t.y;
 }
 
-template <int D, bool CAUSAL, typename T>
+template <int D, bool CAUSAL, typename T, bool P_TMEM>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, T *__restrict__ out,
                   float *__restrict__ lse, int N, int num_q_blocks, float scale, float scale_log2)
 {
-    using C = KCfg<D>;
+    using C = KCfg<D, P_TMEM>;
+    // Early-S order (D = 64, where P has TMEM columns of its own): S_h,j+1 is
+    // issued as soon as sub-tile h's softmax has finished with S_h,j, ahead of
+    // P_h,j V_j, so the two softmax warpgroups need not wait for each other's
+    // products.  With D = 128, P overwrites S_h, so S_h,j+1 follows P_h,j V_j.
+    constexpr bool EARLY_S = P_TMEM && D == 64;
     constexpr int SLOTS = C::SLOTS;
     constexpr int KSTEPS_QK = D / 16;  // UMMA_K = 16 for 16-bit operands
     constexpr int KSTEPS_PV = kBN / 16;
@@ -268,8 +267,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(bar(C::B_SFULL + h), 1);
-            mbar_init(bar(C::B_PFULL + h), 2 * kSubM);
+            mbar_init(bar(C::B_PFULL + h), 4 * 32);
             mbar_init(bar(C::B_OFINAL + h), 1);
+            mbar_init(bar(C::B_SFREE + h), 4 * 32);
+            mbar_init(bar(C::B_OREADY + h), 1);
         }
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = 0;
@@ -285,8 +286,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp >= kMmaWarp) {
-        reg_dealloc<kRegsControl>();
-        if (warp == kTmaWarp && lane == 0) {
+      reg_dealloc<kRegsControl>();
+      if (warp == kTmaWarp && lane == 0) {
             // ---------------- producer ----------------
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -316,37 +317,40 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int s = 0; s < SLOTS; ++s)
                 if (issued > s)
                     drain_bounded(bar(C::B_KVFULL + s), ((issued - 1 - s) / SLOTS) & 1);
-        } else if (warp == kMmaWarp && lane == 0) {
+      } else if (warp == kMmaWarp && lane == 0) {
+        {
             // ---------------- MMA issuer ----------------
             constexpr uint32_t idesc_s = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, kBN, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, D, false, true);
             auto slot_of = [](int L) { return L % SLOTS; };
             auto par_of = [](int L) { return static_cast<uint32_t>((L / SLOTS) & 1); };
-            // Descriptors of the ring's first tile and of Q0; a tile at byte
-            // offset x from them is the same descriptor plus x >> 4 (the start
-            // address field; shared addresses stay below 256 KiB, so no carry).
-            const uint64_t kv_desc_k = make_sdesc_sw128(sbase + C::KV_OFF, 16, 1024);
-            const uint64_t kv_desc_v = make_sdesc_sw128(sbase + C::KV_OFF, kSwAtomBytes, 1024);
-            const uint64_t q_desc = make_sdesc_sw128(sbase + C::Q_OFF, 16, 1024);
             auto issue_s = [&](int h, int j) {
-                const uint64_t kd = kv_desc_k + ((slot_of(2 * j) * C::TILE) >> 4);
-                const uint64_t qd = q_desc + ((h * C::TILE) >> 4);
+                const uint32_t kt = sbase + C::KV_OFF + slot_of(2 * j) * C::TILE;
+                const uint32_t qt = sbase + C::Q_OFF + h * C::TILE;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_QK; ++kk) {
-                    const uint32_t koff = ((kk >> 2) * kSwAtomBytes + (kk & 3) * 32) >> 4;
-                    umma_f16_ss(tmem + h * kBN, qd + koff, kd + koff, idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t koff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
+                    umma_f16_ss(tmem + h * kBN, make_sdesc_sw128(qt + koff, 16, 1024),
+                                make_sdesc_sw128(kt + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int h, int j) {
-                const uint64_t vd = kv_desc_v + ((slot_of(2 * j + 1) * C::TILE) >> 4);
+                const uint32_t vt = sbase + C::KV_OFF + slot_of(2 * j + 1) * C::TILE;
                 const uint32_t od = tmem + kTmemO + h * D;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_PV; ++kk) {
                     // V: MN-major; 16 key rows (2048 B) per K step; the two
                     // 64-column blocks of D = 128 are kSwAtomBytes apart.
-                    // P_h,j: 16-bit in TMEM, two per column, 8 columns per K step.
-                    umma_f16_ts(od, tmem + tmem_p_col<D>(h) + kk * 8, vd + ((kk * 2048) >> 4), idesc_o,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t bd = make_sdesc_sw128(vt + kk * 2048, kSwAtomBytes, 1024);
+                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                    if constexpr (P_TMEM) {
+                        // P_h,j: 16-bit, packed two per column; 8 columns per K step
+                        umma_f16_ts(od, tmem + tmem_p_col<D>(h) + kk * 8, bd, idesc_o, acc);
+                    } else {
+                        const uint32_t pt = sbase + C::P_OFF + h * C::P_TILE;
+                        const uint32_t poff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
+                        umma_f16_ss(od, make_sdesc_sw128(pt + poff, 16, 1024), bd, idesc_o, acc);
+                    }
                 }
             };
             bool ok = wait_bounded(bar(C::B_QFULL), 0, abort_flag) &&
@@ -360,6 +364,47 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 umma_commit(bar(C::B_KVEMPTY + slot_of(0)));
             }
             for (int j = 0; ok && j < nk1; ++j) {
+                if constexpr (EARLY_S) {
+                    bool have_next_k = false;
+                    for (int h = 0; ok && h < 2; ++h) {
+                        const int nkh = h == 0 ? nk0 : nk1;
+                        if (j + 1 >= nkh)
+                            continue;
+                        ok = wait_bounded(bar(C::B_SFREE + h), j & 1, abort_flag);
+                        if (ok && !have_next_k) {
+                            ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 2)), par_of(2 * j + 2),
+                                              abort_flag);
+                            have_next_k = true;
+                        }
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_s(h, j + 1);
+                        umma_commit(bar(C::B_SFULL + h));
+                    }
+                    if (!ok)
+                        break;
+                    if (have_next_k)
+                        umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 2)));  // K_{j+1}: both S products
+                    ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 1)), par_of(2 * j + 1), abort_flag);
+                    for (int h = 0; ok && h < 2; ++h) {
+                        const int nkh = h == 0 ? nk0 : nk1;
+                        if (j >= nkh)
+                            continue;
+                        ok = wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_pv(h, j);
+                        umma_commit(bar(C::B_OREADY + h));
+                        if (j + 1 == nkh)
+                            umma_commit(bar(C::B_OFINAL + h));
+                    }
+                    if (!ok)
+                        break;
+                    umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 1)));  // V_j: both P V products
+                    continue;
+                }
                 ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 1)), par_of(2 * j + 1), abort_flag);
                 bool have_next_k = false;
                 for (int h = 0; ok && h < 2; ++h) {
@@ -396,70 +441,52 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             umma_commit(bar(C::B_DRAIN));
             drain_bounded(bar(C::B_DRAIN), 0);
         }
+      }
     } else {
         reg_alloc<kRegsSoftmax>();
-        // ---------------- softmax: sub-tile h, key half a ----------------
-        const int h = warp >> 3;
-        const int a = (warp >> 2) & 1;
-        const int r = ((warp & 3) << 5) | lane;  // row within the sub-tile == TMEM lane
+        // ---------------- softmax warpgroup h (warps 4h .. 4h+3) ----------------
+        const int h = warp >> 2;
+        const int r = threadIdx.x & 127;  // row within the sub-tile == TMEM lane
         const int qrow = row0 + h * kSubM + r;
         const int nkh = h == 0 ? nk0 : nk1;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(h * kBN + a * kHalf);
-        const uint32_t o_tm = tmem + lane_base + kTmemO + static_cast<uint32_t>(h * D + a * (D / 2));
-        const uint32_t p_tm = tmem + lane_base + tmem_p_col<D>(h) + static_cast<uint32_t>(a * kHalf / 2);
-        // partial-max exchange: [parity][h][half][row]
-        float *xch = reinterpret_cast<float *>(smem + C::X_OFF);
-        auto xslot = [&](int par, int half) { return xch + ((par * 2 + h) * 2 + half) * 128 + r; };
-        const uint32_t pair_bar = 1 + (h << 2) + (warp & 3);  // the two warps sharing these rows
+        const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(h * kBN);
+        const uint32_t o_tm = tmem + lane_base + kTmemO + static_cast<uint32_t>(h * D);
+        const uint32_t p_tm = tmem + lane_base + tmem_p_col<D>(h);
         float m_ref = -INFINITY;  // reference max (raw score units; scale >= 0)
-        float l = 0.f;            // this half's share of the row sum
+        float l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkh; ++j) {
-            // The two warps of a pair pass the same named barriers in the same
-            // order: each reaches the exchange below even when its wait failed
-            // (it then posts NaN), and both leave the loop together after it.
             ok = wait_bounded(bar(C::B_SFULL + h), j & 1, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
-            float s[kHalf];
-            float mh = NAN;
-            float rsum = 0.f;
-            // keys [kbase, kbase + limit) of this half are allowed (limit may be <= 0)
-            const int kbase = j * kBN + a * kHalf;
-            int limit = min(kHalf, N - kbase);
-            if (CAUSAL)
-                limit = min(limit, qrow - kbase + 1);
-            const bool masked = __any_sync(0xffffffffu, limit < kHalf);
-            if (ok) {
-                tc_fence_after();
-                tmem_ld64(s_tm, s);
-                if (masked)
-                    mask_tail(s, limit);
-                // Tile 0 sets the reference max from the exchanged row max.
-                // Later tiles exponentiate against the current reference while
-                // the row max is taken and exchanged; only a row max that
-                // outgrows the reference by more than kRescaleLog2 (rare) sends
-                // the two warps down the redo path.
-                mh = half_max(s);
-                if (j > 0)
-                    rsum = masked ? exp_half<true>(s, limit, scale_log2, -m_ref * scale_log2)
-                                  : exp_half<false>(s, limit, scale_log2, -m_ref * scale_log2);
-            }
-            *xslot(j & 1, a) = mh;
-            named_bar_sync(pair_bar, 64);
-            const float mo = *xslot(j & 1, a ^ 1);
-            ok = __all_sync(0xffffffffu, ok && !isnan(mo));
             if (!ok)
                 break;
-            const float mt = fmaxf(mh, mo);
+            tc_fence_after();
+            float s[kBN];
+            tmem_ld128(s_tm, s);
+            // keys [kbase, kbase + limit) are allowed for this row (limit >= 1)
+            const int kbase = j * kBN;
+            int limit = min(kBN, N - kbase);
+            if (CAUSAL)
+                limit = min(limit, qrow - kbase + 1);
+            const bool masked = __any_sync(0xffffffffu, limit < kBN);
+            if (masked)
+                mask_tail(s, limit);
+            // Tile 0 sets the reference max from its own row max.  Later tiles
+            // exponentiate against the current reference while their row max
+            // is taken; only a row max that outgrows the reference by more than
+            // kRescaleLog2 (rare) sends the warp down the redo path.
             float alpha = 1.f;
+            float rsum;
             if (j == 0) {
-                m_ref = mt;
+                m_ref = row_max(s);
                 alpha = 0.f;
-                rsum = masked ? exp_half<true>(s, limit, scale_log2, -m_ref * scale_log2)
-                              : exp_half<false>(s, limit, scale_log2, -m_ref * scale_log2);
+                rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                              : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
             } else {
-                // identical decision in both halves: mt and m_ref are shared
+                const float mt = row_max(s);
+                rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                              : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
                 const bool grow = (mt - m_ref) * scale_log2 > kRescaleLog2;
                 if (__any_sync(0xffffffffu, grow)) {
                     if (grow) {
@@ -467,29 +494,54 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         m_ref = mt;
                     }
                     // S_h is intact until P_h is written below: redo the tile
-                    tmem_ld64(s_tm, s);
+                    tmem_ld128(s_tm, s);
                     if (masked)
                         mask_tail(s, limit);
-                    rsum = masked ? exp_half<true>(s, limit, scale_log2, -m_ref * scale_log2)
-                                  : exp_half<false>(s, limit, scale_log2, -m_ref * scale_log2);
+                    rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                                  : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
                 }
             }
             l = l * alpha + rsum;
+            if constexpr (EARLY_S) {
+                // S_h,j is no longer needed: let the next S_h product in
+                tc_fence_before();
+                mbar_arrive(bar(C::B_SFREE + h));
+            }
 
-            // P_h,j (this half's 64 keys) rounded to the input dtype
-            {
-                uint32_t w[32];
+            // P_h,j rounded to the input dtype
+            if constexpr (P_TMEM) {
+                uint32_t w[64];
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
+                for (int c = 0; c < 64; ++c)
                     w[c] = DTypeTraits<T>::pack(s[2 * c], s[2 * c + 1]);
-                tmem_st32(p_tm, w);
+                tmem_st64(p_tm, w);
+            } else {
+                const uint32_t pt = sbase + C::P_OFF + h * C::P_TILE;
+#pragma unroll
+                for (int ch = 0; ch < kBN / 8; ++ch) {
+                    const uint32_t w0 = DTypeTraits<T>::pack(s[ch * 8 + 0], s[ch * 8 + 1]);
+                    const uint32_t w1 = DTypeTraits<T>::pack(s[ch * 8 + 2], s[ch * 8 + 3]);
+                    const uint32_t w2 = DTypeTraits<T>::pack(s[ch * 8 + 4], s[ch * 8 + 5]);
+                    const uint32_t w3 = DTypeTraits<T>::pack(s[ch * 8 + 6], s[ch * 8 + 7]);
+                    st_shared_v4(pt + sw128_offset(r, ch), w0, w1, w2, w3);
+                }
+                fence_proxy_async_smem();
             }
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O_h holds P V up to tile j-1 (the S_h,j product, issued after
-                // P_h,j-1 V_{j-1}, has completed) and P_h,j V_j is not issued
-                // before both halves arrive below.  Each half rescales D/2 columns.
-#pragma unroll 1
-                for (int c4 = 0; c4 < D / 64; ++c4) {
+                // O_h must hold P V up to tile j-1, and P_h,j V_j is not issued
+                // before this warpgroup arrives below.  In the early-S order
+                // that product is awaited here (this rare path is the only
+                // reader of O_READY; it can be at most one phase ahead); in the
+                // other order the S_h,j product, issued after it, has completed.
+                if constexpr (EARLY_S) {
+                    ok = wait_bounded(bar(C::B_OREADY + h), (j - 1) & 1, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int c4 = 0; c4 < D / 32; ++c4) {
                     uint32_t u[32];
                     tmem_ld32(o_tm + c4 * 32, u);
 #pragma unroll
@@ -508,48 +560,43 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
 
         // ---------------- epilogue of sub-tile h ----------------
-        // Every softmax thread of the sub-tile reaches both barriers below; a
-        // warp that gave up has set the abort flag first, so after the
-        // sub-tile barrier its eight warps agree on whether the tile is whole.
+        // Every thread of the warpgroup reaches the named barrier; a warp that
+        // gave up has set the abort flag first, so after the barrier the four
+        // warps agree on whether the staged tile is whole.
         if (ok) {
             ok = wait_bounded(bar(C::B_OFINAL + h), 0, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
-        // parity nkh & 1 was last read before the final tile's exchange
-        *xslot(nkh & 1, a) = l;
-        named_bar_sync(pair_bar, 64);
-        const float l_row = l + *xslot(nkh & 1, a ^ 1);
         // Q_h is dead: every product that read it has completed.
         const uint32_t stage = sbase + C::Q_OFF + h * C::TILE;
         if (ok) {
             tc_fence_after();
-            const float inv_l = 1.f / l_row;
-#pragma unroll 1
-            for (int c4 = 0; c4 < D / 64; ++c4) {
+            const float inv_l = 1.f / l;
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
                 uint32_t u[32];
                 tmem_ld32(o_tm + c4 * 32, u);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const float *f = reinterpret_cast<const float *>(u) + q4 * 8;
-                    st_shared_v4(stage + sw128_offset(r, a * (D / 16) + c4 * 4 + q4),
+                    st_shared_v4(stage + sw128_offset(r, c4 * 4 + q4),
                                  DTypeTraits<T>::pack(f[0] * inv_l, f[1] * inv_l),
                                  DTypeTraits<T>::pack(f[2] * inv_l, f[3] * inv_l),
                                  DTypeTraits<T>::pack(f[4] * inv_l, f[5] * inv_l),
                                  DTypeTraits<T>::pack(f[6] * inv_l, f[7] * inv_l));
                 }
             }
-            if (a == 0 && lse != nullptr && qrow < N)
-                lse[static_cast<size_t>(bh) * N + qrow] = m_ref * scale + logf(l_row);
+            if (lse != nullptr && qrow < N)
+                lse[static_cast<size_t>(bh) * N + qrow] = m_ref * scale + logf(l);
         }
-        named_bar_sync(9 + h, 2 * kSubM);
+        named_bar_sync(1 + h, 4 * 32);
         if (*abort_flag == 0) {
             constexpr int CHUNKS_PER_ROW = D / 8;
             const int srow0 = row0 + h * kSubM;
-            const int t = a * kSubM + r;  // 0 .. 255 within the sub-tile
             uint8_t *obase = reinterpret_cast<uint8_t *>(out) +
                              (static_cast<size_t>(bh) * N + srow0) * D * sizeof(T);
 #pragma unroll 4
-            for (int idx = t; idx < kSubM * CHUNKS_PER_ROW; idx += 2 * kSubM) {
+            for (int idx = r; idx < kSubM * CHUNKS_PER_ROW; idx += 4 * 32) {
                 const int row = idx / CHUNKS_PER_ROW;
                 const int ch = idx % CHUNKS_PER_ROW;
                 const uint4 val = ld_shared_v4(stage + sw128_offset(row, ch));
