@@ -508,6 +508,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 mbar_arrive(bar(C::B_SFREE + h));
             }
 
+            if constexpr (EARLY_S) {
+                // P_h,j-1 V_{j-1} must have read P_h before it is overwritten
+                // (and O_h must be complete before a rescale below).
+                if (j > 0) {
+                    ok = wait_bounded(bar(C::B_OREADY + h), (j - 1) & 1, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                }
+            }
+
             // P_h,j rounded to the input dtype
             if constexpr (P_TMEM) {
                 uint32_t w[64];
@@ -530,16 +542,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 // O_h must hold P V up to tile j-1, and P_h,j V_j is not issued
                 // before this warpgroup arrives below.  In the early-S order
-                // that product is awaited here (this rare path is the only
-                // reader of O_READY; it can be at most one phase ahead); in the
-                // other order the S_h,j product, issued after it, has completed.
-                if constexpr (EARLY_S) {
-                    ok = wait_bounded(bar(C::B_OREADY + h), (j - 1) & 1, abort_flag);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                }
+                // that product was awaited above; in the other order the S_h,j
+                // product, issued after it, has completed.
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
                     uint32_t u[32];
