@@ -18,9 +18,10 @@
 //   sub-tile's P V and Q K^T products.
 //   warp 9       TMA producer: Q0, Q1 once; then K_0, V_0, K_1, V_1, ... through
 //                a SLOTS-deep ring of 128B-swizzled shared tiles.
-//   warp 8       MMA issuer (one thread), per key tile j and sub-tile h:
-//                O_h += P_h,j V_j  then  S_h,j+1 = Q_h K_{j+1}^T  (tcgen05.mma,
-//                fp32 accumulators in TMEM).  V is an MN-major B operand.
+//   warps 8, 10  MMA issuers of sub-tiles 0 and 1 (one thread each), per key
+//                tile j: O_h += P_h,j V_j and S_h,j+1 = Q_h K_{j+1}^T
+//                (tcgen05.mma, fp32 accumulators in TMEM).  V is an MN-major
+//                B operand.
 //   warps 4h..4h+3  softmax warpgroup of sub-tile h: thread t owns query row t
 //                = TMEM lane t.  It loads S, masks, takes the row max, updates
 //                the reference max, rescales l and O (in TMEM) by alpha, forms
@@ -55,7 +56,8 @@ constexpr int kSubM = 128;          // rows per sub-tile (one M = 128 MMA; one T
 constexpr int kBM = 2 * kSubM;      // query rows per CTA
 constexpr int kBN = 128;            // keys per K/V tile
 // Three warpgroups: two softmax warpgroups (warps 0-7) and a control
-// warpgroup (warp 8 MMA issuer, warp 9 TMA producer, warps 10-11 idle).
+// warpgroup (warps 8 and 10 MMA issuers of sub-tiles 0 and 1, warp 9 TMA
+// producer, warp 11 idle).
 // Launched at 168 registers per thread (384 x 168 = 64512); the control
 // warpgroup drops to 80 and the softmax warpgroups rise to 208:
 // 256 x 208 + 128 x 80 = 63488 <= 64512.
@@ -97,8 +99,8 @@ struct KCfg {
     static constexpr int B_OFINAL = B_PFULL + 2;       // two
     static constexpr int B_SFREE = B_OFINAL + 2;       // two (early-S order only)
     static constexpr int B_OREADY = B_SFREE + 2;       // two (early-S order only)
-    static constexpr int B_DRAIN = B_OREADY + 2;
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int B_DRAIN = B_OREADY + 2;       // two (one per MMA issuer)
+    static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // TMEM base address, abort flag
     static constexpr int SMEM_USED = SLOT_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         mbar_init(bar(C::B_QFULL), 1);
         for (int s = 0; s < SLOTS; ++s) {
             mbar_init(bar(C::B_KVFULL + s), 1);
-            mbar_init(bar(C::B_KVEMPTY + s), 1);
+            mbar_init(bar(C::B_KVEMPTY + s), 2);  // one release per MMA issuer
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(bar(C::B_SFULL + h), 1);
@@ -272,7 +274,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(bar(C::B_SFREE + h), 4 * 32);
             mbar_init(bar(C::B_OREADY + h), 1);
         }
-        mbar_init(bar(C::B_DRAIN), 1);
+        mbar_init(bar(C::B_DRAIN + 0), 1);
+        mbar_init(bar(C::B_DRAIN + 1), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -317,26 +320,32 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int s = 0; s < SLOTS; ++s)
                 if (issued > s)
                     drain_bounded(bar(C::B_KVFULL + s), ((issued - 1 - s) / SLOTS) & 1);
-      } else if (warp == kMmaWarp && lane == 0) {
-        {
-            // ---------------- MMA issuer ----------------
+      } else if ((warp == kMmaWarp || warp == kMmaWarp + 2) && lane == 0) {
+            // ---------------- MMA issuer of sub-tile h ----------------
+            // One issuing thread per sub-tile: a thread that issues tcgen05.mma
+            // is held for about the product's execution time, so with two
+            // issuers one keeps the tensor core fed while the other waits on
+            // its barriers.  K/V slots are released by both issuers.
+            const int h = (warp == kMmaWarp) ? 0 : 1;
+            const int nkh = h == 0 ? nk0 : nk1;
             constexpr uint32_t idesc_s = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, kBN, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, D, false, true);
             auto slot_of = [](int L) { return L % SLOTS; };
             auto par_of = [](int L) { return static_cast<uint32_t>((L / SLOTS) & 1); };
-            auto issue_s = [&](int h, int j) {
+            const uint32_t d_s = tmem + h * kBN;
+            const uint32_t d_o = tmem + kTmemO + h * D;
+            auto issue_s = [&](int j) {
                 const uint32_t kt = sbase + C::KV_OFF + slot_of(2 * j) * C::TILE;
                 const uint32_t qt = sbase + C::Q_OFF + h * C::TILE;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_QK; ++kk) {
                     const uint32_t koff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
-                    umma_f16_ss(tmem + h * kBN, make_sdesc_sw128(qt + koff, 16, 1024),
+                    umma_f16_ss(d_s, make_sdesc_sw128(qt + koff, 16, 1024),
                                 make_sdesc_sw128(kt + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int h, int j) {
+            auto issue_pv = [&](int j) {
                 const uint32_t vt = sbase + C::KV_OFF + slot_of(2 * j + 1) * C::TILE;
-                const uint32_t od = tmem + kTmemO + h * D;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_PV; ++kk) {
                     // V: MN-major; 16 key rows (2048 B) per K step; the two
@@ -345,102 +354,75 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                     if constexpr (P_TMEM) {
                         // P_h,j: 16-bit, packed two per column; 8 columns per K step
-                        umma_f16_ts(od, tmem + tmem_p_col<D>(h) + kk * 8, bd, idesc_o, acc);
+                        umma_f16_ts(d_o, tmem + tmem_p_col<D>(h) + kk * 8, bd, idesc_o, acc);
                     } else {
                         const uint32_t pt = sbase + C::P_OFF + h * C::P_TILE;
                         const uint32_t poff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
-                        umma_f16_ss(od, make_sdesc_sw128(pt + poff, 16, 1024), bd, idesc_o, acc);
+                        umma_f16_ss(d_o, make_sdesc_sw128(pt + poff, 16, 1024), bd, idesc_o, acc);
                     }
                 }
             };
-            bool ok = wait_bounded(bar(C::B_QFULL), 0, abort_flag) &&
-                      wait_bounded(bar(C::B_KVFULL + slot_of(0)), par_of(0), abort_flag);
+            auto wait_load = [&](int L) {
+                return wait_bounded(bar(C::B_KVFULL + slot_of(L)), par_of(L), abort_flag);
+            };
+            bool ok = wait_bounded(bar(C::B_QFULL), 0, abort_flag) && wait_load(0);
             if (ok) {
                 tc_fence_after();
-                issue_s(0, 0);
-                umma_commit(bar(C::B_SFULL + 0));
-                issue_s(1, 0);
-                umma_commit(bar(C::B_SFULL + 1));
+                issue_s(0);
+                umma_commit(bar(C::B_SFULL + h));
                 umma_commit(bar(C::B_KVEMPTY + slot_of(0)));
             }
-            for (int j = 0; ok && j < nk1; ++j) {
+            for (int j = 0; ok && j < nkh; ++j) {
                 if constexpr (EARLY_S) {
-                    bool have_next_k = false;
-                    for (int h = 0; ok && h < 2; ++h) {
-                        const int nkh = h == 0 ? nk0 : nk1;
-                        if (j + 1 >= nkh)
-                            continue;
-                        ok = wait_bounded(bar(C::B_SFREE + h), j & 1, abort_flag);
-                        if (ok && !have_next_k) {
-                            ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 2)), par_of(2 * j + 2),
-                                              abort_flag);
-                            have_next_k = true;
-                        }
+                    if (j + 1 < nkh) {
+                        ok = wait_bounded(bar(C::B_SFREE + h), j & 1, abort_flag) && wait_load(2 * j + 2);
                         if (!ok)
                             break;
                         tc_fence_after();
-                        issue_s(h, j + 1);
+                        issue_s(j + 1);
                         umma_commit(bar(C::B_SFULL + h));
+                        umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 2)));
                     }
-                    if (!ok)
-                        break;
-                    if (have_next_k)
-                        umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 2)));  // K_{j+1}: both S products
-                    ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 1)), par_of(2 * j + 1), abort_flag);
-                    for (int h = 0; ok && h < 2; ++h) {
-                        const int nkh = h == 0 ? nk0 : nk1;
-                        if (j >= nkh)
-                            continue;
-                        ok = wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
-                        if (!ok)
-                            break;
-                        tc_fence_after();
-                        issue_pv(h, j);
-                        umma_commit(bar(C::B_OREADY + h));
-                        if (j + 1 == nkh)
-                            umma_commit(bar(C::B_OFINAL + h));
-                    }
-                    if (!ok)
-                        break;
-                    umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 1)));  // V_j: both P V products
-                    continue;
-                }
-                ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 1)), par_of(2 * j + 1), abort_flag);
-                bool have_next_k = false;
-                for (int h = 0; ok && h < 2; ++h) {
-                    const int nkh = h == 0 ? nk0 : nk1;
-                    if (j >= nkh)
-                        continue;
-                    ok = wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
+                    ok = wait_load(2 * j + 1) && wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
                     if (!ok)
                         break;
                     tc_fence_after();
-                    issue_pv(h, j);
+                    issue_pv(j);
+                    umma_commit(bar(C::B_OREADY + h));
+                    umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 1)));
+                    if (j + 1 == nkh)
+                        umma_commit(bar(C::B_OFINAL + h));
+                } else {
+                    ok = wait_load(2 * j + 1) && wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    issue_pv(j);
+                    umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 1)));
                     if (j + 1 < nkh) {
-                        if (!have_next_k) {
-                            ok = wait_bounded(bar(C::B_KVFULL + slot_of(2 * j + 2)), par_of(2 * j + 2),
-                                              abort_flag);
-                            if (!ok)
-                                break;
-                            tc_fence_after();
-                            have_next_k = true;
-                        }
-                        issue_s(h, j + 1);
+                        ok = wait_load(2 * j + 2);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_s(j + 1);
                         umma_commit(bar(C::B_SFULL + h));
+                        umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 2)));
                     } else {
                         umma_commit(bar(C::B_OFINAL + h));
                     }
                 }
-                if (!ok)
-                    break;
-                umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 1)));  // V_j: both P V products issued
-                if (have_next_k)
-                    umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 2)));  // K_{j+1}: both S products
             }
-            // every MMA issued above has completed once this arrives
-            umma_commit(bar(C::B_DRAIN));
-            drain_bounded(bar(C::B_DRAIN), 0);
-        }
+            // Causal sub-tile 0 ends before sub-tile 1: release the K/V tiles
+            // it does not read (after each lands, so the arrival counts for
+            // that use of the slot).
+            for (int L = 2 * nkh; ok && L < 2 * nk1; ++L) {
+                ok = wait_load(L);
+                if (ok)
+                    mbar_arrive(bar(C::B_KVEMPTY + slot_of(L)));
+            }
+            // every MMA this thread issued has completed once this arrives
+            umma_commit(bar(C::B_DRAIN + h));
+            drain_bounded(bar(C::B_DRAIN + h), 0);
       }
     } else {
         reg_alloc<kRegsSoftmax>();
