@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // P_h,j V_j, so the two softmax warpgroups need not wait for each other's
     // products.  With D = 128, P overwrites S_h, so S_h,j+1 follows P_h,j V_j.
     constexpr bool EARLY_S = P_TMEM && D == 64;
+    constexpr int NUM_ISSUERS = EARLY_S ? 2 : 1;
     constexpr int SLOTS = C::SLOTS;
     constexpr int KSTEPS_QK = D / 16;  // UMMA_K = 16 for 16-bit operands
     constexpr int KSTEPS_PV = kBN / 16;
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         mbar_init(bar(C::B_QFULL), 1);
         for (int s = 0; s < SLOTS; ++s) {
             mbar_init(bar(C::B_KVFULL + s), 1);
-            mbar_init(bar(C::B_KVEMPTY + s), 2);  // one release per MMA issuer
+            mbar_init(bar(C::B_KVEMPTY + s), NUM_ISSUERS);  // one release per MMA issuer
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(bar(C::B_SFULL + h), 1);
@@ -320,37 +321,48 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int s = 0; s < SLOTS; ++s)
                 if (issued > s)
                     drain_bounded(bar(C::B_KVFULL + s), ((issued - 1 - s) / SLOTS) & 1);
-      } else if ((warp == kMmaWarp || warp == kMmaWarp + 2) && lane == 0) {
-            // ---------------- MMA issuer of sub-tile h ----------------
-            // One issuing thread per sub-tile: a thread that issues tcgen05.mma
-            // is held for about the product's execution time, so with two
-            // issuers one keeps the tensor core fed while the other waits on
-            // its barriers.  K/V slots are released by both issuers.
-            const int h = (warp == kMmaWarp) ? 0 : 1;
-            const int nkh = h == 0 ? nk0 : nk1;
+      } else if (lane == 0 && (warp == kMmaWarp || (NUM_ISSUERS == 2 && warp == kMmaWarp + 2))) {
+            // ---------------- MMA issuer(s) ----------------
+            // A thread that issues tcgen05.mma is held for about the product's
+            // execution time, so its own barrier waits leave the tensor core
+            // idle.  With D = 64 (short products, early-S order) each sub-tile
+            // gets its own issuer (warps 8 and 10), so one issues while the
+            // other waits.  With D = 128 one issuer serves both sub-tiles in a
+            // fixed ping-pong order, which keeps each sub-tile's products
+            // together.  Each issuer releases every K/V load once (after its
+            // products read it, or after it lands if it reads none of it).
+            const int me = (warp == kMmaWarp) ? 0 : 1;
+            const int h_lo = NUM_ISSUERS == 2 ? me : 0;
+            const int h_hi = NUM_ISSUERS == 2 ? me + 1 : 2;
+            const int nk_mine = NUM_ISSUERS == 2 ? (me == 0 ? nk0 : nk1) : nk1;
             constexpr uint32_t idesc_s = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, kBN, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, D, false, true);
             auto slot_of = [](int L) { return L % SLOTS; };
             auto par_of = [](int L) { return static_cast<uint32_t>((L / SLOTS) & 1); };
-            const uint32_t d_s = tmem + h * kBN;
-            const uint32_t d_o = tmem + kTmemO + h * D;
-            auto issue_s = [&](int j) {
-                const uint32_t kt = sbase + C::KV_OFF + slot_of(2 * j) * C::TILE;
-                const uint32_t qt = sbase + C::Q_OFF + h * C::TILE;
+            // Descriptors of the ring's first tile and of Q0: a tile at byte
+            // offset x from them is the same descriptor plus x >> 4 (the start
+            // address field; shared addresses stay below 256 KiB, no carry).
+            const uint64_t desc_k0 = make_sdesc_sw128(sbase + C::KV_OFF, 16, 1024);
+            const uint64_t desc_v0 = make_sdesc_sw128(sbase + C::KV_OFF, kSwAtomBytes, 1024);
+            const uint64_t desc_q0 = make_sdesc_sw128(sbase + C::Q_OFF, 16, 1024);
+            auto nk_of = [&](int h) { return h == 0 ? nk0 : nk1; };
+            auto issue_s = [&](int h, int j) {
+                const uint64_t kd = desc_k0 + static_cast<uint32_t>((slot_of(2 * j) * C::TILE) >> 4);
+                const uint64_t qd = desc_q0 + static_cast<uint32_t>((h * C::TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_QK; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
-                    umma_f16_ss(d_s, make_sdesc_sw128(qt + koff, 16, 1024),
-                                make_sdesc_sw128(kt + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t koff = static_cast<uint32_t>(((kk >> 2) * kSwAtomBytes + (kk & 3) * 32) >> 4);
+                    umma_f16_ss(tmem + h * kBN, qd + koff, kd + koff, idesc_s, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int j) {
-                const uint32_t vt = sbase + C::KV_OFF + slot_of(2 * j + 1) * C::TILE;
+            auto issue_pv = [&](int h, int j) {
+                const uint64_t vd = desc_v0 + static_cast<uint32_t>((slot_of(2 * j + 1) * C::TILE) >> 4);
+                const uint32_t d_o = tmem + kTmemO + h * D;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_PV; ++kk) {
                     // V: MN-major; 16 key rows (2048 B) per K step; the two
                     // 64-column blocks of D = 128 are kSwAtomBytes apart.
-                    const uint64_t bd = make_sdesc_sw128(vt + kk * 2048, kSwAtomBytes, 1024);
+                    const uint64_t bd = vd + static_cast<uint32_t>((kk * 2048) >> 4);
                     const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                     if constexpr (P_TMEM) {
                         // P_h,j: 16-bit, packed two per column; 8 columns per K step
@@ -365,64 +377,97 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             auto wait_load = [&](int L) {
                 return wait_bounded(bar(C::B_KVFULL + slot_of(L)), par_of(L), abort_flag);
             };
+            // Releases load L: after this issuer's products that read it
+            // (commit), or, when none did, as soon as it has landed.
+            auto release = [&](int L, bool used) -> bool {
+                if (used) {
+                    umma_commit(bar(C::B_KVEMPTY + slot_of(L)));
+                    return true;
+                }
+                if (!wait_load(L))
+                    return false;
+                mbar_arrive(bar(C::B_KVEMPTY + slot_of(L)));
+                return true;
+            };
             bool ok = wait_bounded(bar(C::B_QFULL), 0, abort_flag) && wait_load(0);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
-                umma_commit(bar(C::B_SFULL + h));
-                umma_commit(bar(C::B_KVEMPTY + slot_of(0)));
+                for (int h = h_lo; h < h_hi; ++h) {
+                    issue_s(h, 0);
+                    umma_commit(bar(C::B_SFULL + h));
+                }
+                release(0, true);
             }
-            for (int j = 0; ok && j < nkh; ++j) {
+            for (int j = 0; ok && j < nk1; ++j) {
                 if constexpr (EARLY_S) {
-                    if (j + 1 < nkh) {
-                        ok = wait_bounded(bar(C::B_SFREE + h), j & 1, abort_flag) && wait_load(2 * j + 2);
+                    // next S products first, then this tile's P V products
+                    bool k_used = false;
+                    for (int h = h_lo; ok && h < h_hi; ++h) {
+                        if (j + 1 >= nk_of(h))
+                            continue;
+                        ok = wait_bounded(bar(C::B_SFREE + h), j & 1, abort_flag) &&
+                             (k_used || wait_load(2 * j + 2));
                         if (!ok)
                             break;
                         tc_fence_after();
-                        issue_s(j + 1);
+                        issue_s(h, j + 1);
                         umma_commit(bar(C::B_SFULL + h));
-                        umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 2)));
+                        k_used = true;
                     }
-                    ok = wait_load(2 * j + 1) && wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    issue_pv(j);
-                    umma_commit(bar(C::B_OREADY + h));
-                    umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 1)));
-                    if (j + 1 == nkh)
-                        umma_commit(bar(C::B_OFINAL + h));
+                    if (ok && j + 1 < nk1)
+                        ok = release(2 * j + 2, k_used);
+                    bool v_used = false;
+                    for (int h = h_lo; ok && h < h_hi; ++h) {
+                        if (j >= nk_of(h))
+                            continue;
+                        ok = (v_used || wait_load(2 * j + 1)) &&
+                             wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_pv(h, j);
+                        umma_commit(bar(C::B_OREADY + h));
+                        if (j + 1 == nk_of(h))
+                            umma_commit(bar(C::B_OFINAL + h));
+                        v_used = true;
+                    }
+                    if (ok)
+                        ok = release(2 * j + 1, v_used);
                 } else {
-                    ok = wait_load(2 * j + 1) && wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    issue_pv(j);
-                    umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 1)));
-                    if (j + 1 < nkh) {
-                        ok = wait_load(2 * j + 2);
+                    // per sub-tile: P V of this tile, then the next S product
+                    bool v_used = false, k_used = false;
+                    for (int h = h_lo; ok && h < h_hi; ++h) {
+                        if (j >= nk_of(h))
+                            continue;
+                        ok = (v_used || wait_load(2 * j + 1)) &&
+                             wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
                         if (!ok)
                             break;
                         tc_fence_after();
-                        issue_s(j + 1);
-                        umma_commit(bar(C::B_SFULL + h));
-                        umma_commit(bar(C::B_KVEMPTY + slot_of(2 * j + 2)));
-                    } else {
-                        umma_commit(bar(C::B_OFINAL + h));
+                        issue_pv(h, j);
+                        v_used = true;
+                        if (j + 1 < nk_of(h)) {
+                            ok = k_used || wait_load(2 * j + 2);
+                            if (!ok)
+                                break;
+                            tc_fence_after();
+                            issue_s(h, j + 1);
+                            umma_commit(bar(C::B_SFULL + h));
+                            k_used = true;
+                        } else {
+                            umma_commit(bar(C::B_OFINAL + h));
+                        }
                     }
+                    if (ok)
+                        ok = release(2 * j + 1, v_used);
+                    if (ok && j + 1 < nk1)
+                        ok = release(2 * j + 2, k_used);
                 }
             }
-            // Causal sub-tile 0 ends before sub-tile 1: release the K/V tiles
-            // it does not read (after each lands, so the arrival counts for
-            // that use of the slot).
-            for (int L = 2 * nkh; ok && L < 2 * nk1; ++L) {
-                ok = wait_load(L);
-                if (ok)
-                    mbar_arrive(bar(C::B_KVEMPTY + slot_of(L)));
-            }
+            (void)nk_mine;
             // every MMA this thread issued has completed once this arrives
-            umma_commit(bar(C::B_DRAIN + h));
-            drain_bounded(bar(C::B_DRAIN + h), 0);
+            umma_commit(bar(C::B_DRAIN + me));
+            drain_bounded(bar(C::B_DRAIN + me), 0);
       }
     } else {
         reg_alloc<kRegsSoftmax>();
