@@ -242,11 +242,16 @@ class OracleTimer:
         return time.perf_counter() - t0, flops
 
     def rows_for_seconds(self, seconds):
-        """Calibrate: rows whose oracle time is about `seconds`."""
-        probe = oracle_sample_rows(self.meta, 2 * self.threads, seed=1)
-        dt, _ = self.run(probe)
-        per_row = max(dt / len(probe), 1e-7)
-        return max(1, int(seconds / per_row))
+        """Calibrate: rows whose oracle time is about `seconds` (at most all rows)."""
+        total = self.meta["B"] * self.meta["H"] * self.meta["N"]
+        n = min(total, 64 * self.threads)
+        while True:
+            dt, _ = self.run(oracle_sample_rows(self.meta, n, seed=1))
+            if dt >= 0.25 or n >= total:
+                break
+            n = min(total, n * 4)
+        per_row = max(dt / n, 1e-9)
+        return max(1, min(total, int(seconds / per_row)))
 
 
 def cpu_baseline_obj(timer, seconds, seed=99):
@@ -448,7 +453,7 @@ def run_reference(args, q, k, v, meta, variants, config, step_flops, world, rank
     timer = OracleTimer(q, k, v, meta, variants)
     budget = max(30.0, min(150.0, args.cpu_seconds * 8))
     n_steps = args.steps + max(args.warmup, 0)
-    rows_per_step = max(1, timer.rows_for_seconds(budget / max(n_steps, 1)))
+    rows_per_step = timer.rows_for_seconds(budget / max(n_steps, 1))
     for i in range(max(args.warmup, 0)):
         timer.run(oracle_sample_rows(meta, rows_per_step, seed=500 + i))
     tot_t, tot_f = 0.0, 0.0
