@@ -8,10 +8,11 @@ computation runs in the library's kernel.  There is no CPU or eager fallback:
 without the built library, or off a CUDA device, calls raise ``FAError``.
 """
 from ._lib import (FA_BF16, FA_FP16, FAError, fa_abi_version, fa_fwd_raw,
-                   fa_last_device_status, fa_status_str, lib_path, load)
+                   fa_last_device_status, fa_selftest_wait_timeout, fa_status_str, lib_path,
+                   load)
 
-__all__ = ["fa_fwd", "fa_fwd_raw", "fa_last_device_status", "fa_status_str", "fa_abi_version",
-           "FAError", "load", "lib_path"]
+__all__ = ["fa_fwd", "fa_fwd_raw", "fa_last_device_status", "fa_selftest_wait_timeout",
+           "fa_status_str", "fa_abi_version", "FAError", "load", "lib_path"]
 
 
 def _dtype_code(t):

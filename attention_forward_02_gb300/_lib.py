@@ -19,7 +19,8 @@ FA_FP16 = 0
 FA_BF16 = 1
 
 # every symbol include/fa.h declares
-EXPORTS = ("fa_fwd", "fa_last_device_status", "fa_status_str", "fa_abi_version")
+EXPORTS = ("fa_fwd", "fa_last_device_status", "fa_selftest_wait_timeout", "fa_status_str",
+           "fa_abi_version")
 
 _lib = None
 
@@ -52,6 +53,8 @@ def load(path=None):
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_last_device_status.restype = i
     lib.fa_last_device_status.argtypes = [vp]
+    lib.fa_selftest_wait_timeout.restype = i
+    lib.fa_selftest_wait_timeout.argtypes = [i, vp]
     lib.fa_status_str.restype = ctypes.c_char_p
     lib.fa_status_str.argtypes = [i]
     lib.fa_abi_version.restype = i
@@ -71,6 +74,10 @@ def fa_fwd_raw(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream):
 
 def fa_last_device_status(stream=None):
     return load().fa_last_device_status(stream)
+
+
+def fa_selftest_wait_timeout(limit_us, stream=None):
+    return load().fa_selftest_wait_timeout(int(limit_us), stream)
 
 
 def fa_status_str(status):

@@ -205,7 +205,25 @@ fa_status_t fa_last_device_status(void *stream)
         return FA_ERR_CUDA;
     if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess)
         return FA_ERR_CUDA;
+    if (word & ~fa::kStatusTimeout)
+        return FA_ERR_CUDA;  // a self-test wait did not behave as required
     return (word & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status_t fa_selftest_wait_timeout(int limit_us, void *stream)
+{
+    if (limit_us < 1 || limit_us > 1000000)
+        return FA_ERR_INVALID_ARG;
+    int dev = -1;
+    int clock_khz = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, dev) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (clock_khz <= 0)
+        clock_khz = 2000000;
+    const long long cycles = static_cast<long long>(limit_us) * (clock_khz / 1000);
+    fa::fa_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(cycles);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 const char *fa_status_str(fa_status_t status)

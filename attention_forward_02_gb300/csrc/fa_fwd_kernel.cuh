@@ -131,7 +131,8 @@ struct DTypeTraits<__nv_bfloat16> {
 
 // Bounded wait.  Returns false if the CTA is aborting or the limit expired
 // (then the abort flag and the device status word are set).
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             long long limit_cycles = kWaitLimitCycles)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -141,7 +142,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
             return true;
         if (*abort_flag)
             return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit_cycles) {
             *abort_flag = 1;
             atomicOr(&g_fa_status, kStatusTimeout);
             return false;
@@ -644,6 +645,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Failure-path self-test: one warp waits on an mbarrier that nothing ever
+// arrives on.  The bounded wait must give up after limit_cycles, set the CTA
+// abort flag and record kStatusTimeout in the device status word.
+__global__ void fa_selftest_wait_kernel(long long limit_cycles)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const bool ok = wait_bounded(smem_u32(&bar), 0, &abort_flag, limit_cycles);
+        if (ok || abort_flag != 1)
+            atomicOr(&g_fa_status, 2u);  // the wait did not behave as required
     }
 }
 

@@ -48,6 +48,8 @@ def parse_args():
                     help="comma list of noncausal/causal launches per step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target host seconds for the cpu_baseline / reference sample")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="target total host seconds of the --impl reference run")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -451,7 +453,7 @@ def run_reference(args, q, k, v, meta, variants, config, step_flops, world, rank
     if rank != 0:
         return
     timer = OracleTimer(q, k, v, meta, variants)
-    budget = max(30.0, min(150.0, args.cpu_seconds * 8))
+    budget = max(0.5, args.ref_seconds)
     n_steps = args.steps + max(args.warmup, 0)
     rows_per_step = timer.rows_for_seconds(budget / max(n_steps, 1))
     for i in range(max(args.warmup, 0)):

@@ -94,6 +94,17 @@ FA_API fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, 
  */
 FA_API fa_status_t fa_last_device_status(void *stream);
 
+/*
+ * fa_selftest_wait_timeout -- exercises the failure path without a GPU fault.
+ * Launches one small kernel on `stream` whose bounded mbarrier wait (the same
+ * wait the attention kernels use) waits on a barrier that nothing arrives on.
+ * After about limit_us microseconds (1 .. 1e6) the wait gives up and records a
+ * timeout in the device status word; fa_last_device_status then returns
+ * FA_ERR_TIMEOUT (or FA_ERR_CUDA if the wait misbehaved).  Nothing hangs or
+ * traps, and the CUDA context stays usable.  Returns FA_OK once launched.
+ */
+FA_API fa_status_t fa_selftest_wait_timeout(int limit_us, void *stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 FA_API const char *fa_status_str(fa_status_t status);
 

@@ -74,6 +74,11 @@ def test_argument_checks(lib, kwargs, status):
     assert call(**kwargs) == status
 
 
+def test_selftest_rejects_bad_limit_before_cuda(lib):
+    assert fa.fa_selftest_wait_timeout(0) == 1
+    assert fa.fa_selftest_wait_timeout(2_000_000) == 1
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(fa.FAError):
