@@ -7,11 +7,12 @@ PyTorch only supplies device memory and the stream; every step of the
 computation runs in the library's kernel.  There is no CPU or eager fallback:
 without the built library, or off a CUDA device, calls raise ``FAError``.
 """
-from ._lib import (FA_BF16, FA_FP16, FAError, fa_abi_version, fa_fwd_raw,
-                   fa_last_device_status, fa_selftest_wait_timeout, fa_status_str, lib_path,
-                   load)
+from ._lib import (FA_BF16, FA_FP16, FAError, fa1_fwd_raw, fa1_fwd_workspace_size,
+                   fa_abi_version, fa_fwd_raw, fa_last_device_status, fa_selftest_wait_timeout,
+                   fa_status_str, lib_path, load)
 
-__all__ = ["fa_fwd", "fa_fwd_raw", "fa_last_device_status", "fa_selftest_wait_timeout",
+__all__ = ["fa_fwd", "fa_fwd_raw", "fa1_fwd", "fa1_fwd_raw", "fa1_fwd_workspace_size",
+           "fa_last_device_status", "fa_selftest_wait_timeout",
            "fa_status_str", "fa_abi_version", "FAError", "load", "lib_path"]
 
 
@@ -22,6 +23,60 @@ def _dtype_code(t):
     if t.dtype == torch.bfloat16:
         return FA_BF16
     raise FAError(2, "dtype must be float16 or bfloat16, got %s" % t.dtype)
+
+
+def _check_qkv(q, k, v):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise FAError(1, "%s must be a CUDA tensor" % name)
+        if t.dim() != 4 or not t.is_contiguous():
+            raise FAError(1, "%s must be a contiguous [B, H, N, d] tensor" % name)
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise FAError(1, "q, k, v must share shape and dtype")
+
+
+def _outputs(q, o, lse, return_lse):
+    import torch
+    B, H, N, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    elif o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous() or not o.is_cuda:
+        raise FAError(1, "o must be a contiguous CUDA tensor shaped and typed like q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    if lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32
+                            or not lse.is_contiguous() or not lse.is_cuda):
+        raise FAError(1, "lse must be a contiguous CUDA float32 tensor of shape [B, H, N]")
+    return o, lse
+
+
+def fa1_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, return_lse=True, workspace=None,
+            stream=None):
+    """The FA1-structured baseline (same arguments and results as fa_fwd).
+
+    workspace: optional CUDA uint8 tensor of at least fa1_fwd_workspace_size
+    bytes; allocated with torch when None."""
+    import torch
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    code = _dtype_code(q)
+    if scale is None:
+        scale = float(d) ** -0.5
+    o, lse = _outputs(q, o, lse, return_lse)
+    need = fa1_fwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa1_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
+                         int(bool(causal)), code, stream.cuda_stream)
+    if st != 0:
+        raise FAError(st, "fa1_fwd")
+    return o, lse
 
 
 def fa_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, return_lse=True, stream=None):

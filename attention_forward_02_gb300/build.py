@@ -16,7 +16,8 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB = os.path.join(OUT_DIR, LIB_NAME)
 SOURCES = [os.path.join(CSRC, "fa_fwd.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "sm100_ptx.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa1_fwd_kernel.cuh",
+                                                  "sm100_ptx.cuh")] + [
     os.path.join(INCLUDE, "fa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa1_fwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace {
@@ -37,6 +38,14 @@ cudaError_t set_smem_attr()
     return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, T, kPInTmem>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 fa::KCfg<D, kPInTmem>::SMEM_ALLOC);
+}
+
+template <int D, bool CAUSAL, typename T>
+cudaError_t set_smem_attr_fa1()
+{
+    return cudaFuncSetAttribute(fa::fa1::fa1_fwd_kernel<D, CAUSAL, T>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fa::fa1::Cfg<D>::SMEM_ALLOC);
 }
 
 void init_device(int dev, DeviceState &st)
@@ -69,6 +78,14 @@ void init_device(int dev, DeviceState &st)
     if (e == cudaSuccess) e = set_smem_attr<64, true, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr<128, false, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr<128, true, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<64, false, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<64, true, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<128, false, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<128, true, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<64, false, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<64, true, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<128, false, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<128, true, __nv_bfloat16>();
     st.init_status = (e == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -118,16 +135,26 @@ fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+template <int D, bool CAUSAL, typename T>
+fa_status_t launch_fa1(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
+                       float *lse, float *ws, int BH, int N, float scale, cudaStream_t stream)
+{
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    fa::fa1::fa1_fwd_kernel<D, CAUSAL, T>
+        <<<static_cast<unsigned>(BH), fa::fa1::kThreads, fa::fa1::Cfg<D>::SMEM_ALLOC, stream>>>(
+            mq, mk, mv, static_cast<T *>(o), lse, ws, N, scale, scale_log2);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 bool overlaps(uintptr_t a, size_t na, uintptr_t b, size_t nb) { return a < b + nb && b < a + na; }
 
-}  // namespace
-
-extern "C" {
-
-fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-                   int N, int d, float scale, int causal, fa_dtype_t dtype, void *stream)
+// Checks shared by the entry points; nothing here calls CUDA.  Sets *empty for
+// a problem with nothing to compute.
+fa_status_t check_args(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                       int B, int H, int N, int d, float scale, int causal, fa_dtype_t dtype,
+                       bool *empty)
 {
-    // ---- argument checks (no CUDA call before they pass) ----
+    *empty = false;
     if (B < 0 || H < 0 || N < 0)
         return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1)
@@ -140,8 +167,10 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
         return FA_ERR_UNSUPPORTED;
     if (scale < 0.f)
         return FA_ERR_UNSUPPORTED;
-    if (B == 0 || H == 0 || N == 0)
-        return FA_OK;  // empty problem
+    if (B == 0 || H == 0 || N == 0) {
+        *empty = true;  // empty problem
+        return FA_OK;
+    }
     if (!q || !k || !v || !o)
         return FA_ERR_INVALID_ARG;
     const long long BH = static_cast<long long>(B) * H;
@@ -168,17 +197,37 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
             overlaps(ul, lbytes, reinterpret_cast<uintptr_t>(v), bytes))
             return FA_ERR_INVALID_ARG;
     }
+    return FA_OK;
+}
 
-    // ---- device state, descriptors, launch ----
+// Device state plus the three TMA descriptors of Q, K, V.
+fa_status_t prepare(const void *q, const void *k, const void *v, int BH, int N, int d,
+                    fa_dtype_t dtype, CUtensorMap *mq, CUtensorMap *mk, CUtensorMap *mv)
+{
     DeviceState *st = nullptr;
     fa_status_t s = device_state(&st);
     if (s != FA_OK)
         return s;
+    if ((s = encode_qkv_map(st->encode, mq, q, BH, N, d, dtype)) != FA_OK) return s;
+    if ((s = encode_qkv_map(st->encode, mk, k, BH, N, d, dtype)) != FA_OK) return s;
+    return encode_qkv_map(st->encode, mv, v, BH, N, d, dtype);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int N, int d, float scale, int causal, fa_dtype_t dtype, void *stream)
+{
+    bool empty = false;
+    fa_status_t s = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
+    if (s != FA_OK || empty)
+        return s;
+    const int bh = B * H;
     CUtensorMap mq, mk, mv;
-    const int bh = static_cast<int>(BH);
-    if ((s = encode_qkv_map(st->encode, &mq, q, bh, N, d, dtype)) != FA_OK) return s;
-    if ((s = encode_qkv_map(st->encode, &mk, k, bh, N, d, dtype)) != FA_OK) return s;
-    if ((s = encode_qkv_map(st->encode, &mv, v, bh, N, d, dtype)) != FA_OK) return s;
+    if ((s = prepare(q, k, v, bh, N, d, dtype, &mq, &mk, &mv)) != FA_OK)
+        return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (dtype == FA_FP16) {
         if (d == 64)
@@ -192,6 +241,55 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
                       : launch<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs);
     return causal ? launch<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs)
                   : launch<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs);
+}
+
+size_t fa1_fwd_workspace_size(int B, int H, int N, int d)
+{
+    if (B < 0 || H < 0 || N < 0 || (d != 64 && d != 128))
+        return 0;
+    return fa::fa1::workspace_floats(static_cast<long long>(B) * H, N, d) * sizeof(float);
+}
+
+fa_status_t fa1_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                    void *workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                    float scale, int causal, fa_dtype_t dtype, void *stream)
+{
+    bool empty = false;
+    fa_status_t s = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
+    if (s != FA_OK || empty)
+        return s;
+    const size_t need = fa1_fwd_workspace_size(B, H, N, d);
+    if (!workspace || workspace_bytes < need)
+        return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u)
+        return FA_ERR_MISALIGNED;
+    const size_t bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const uintptr_t uw = reinterpret_cast<uintptr_t>(workspace);
+    if (overlaps(uw, need, reinterpret_cast<uintptr_t>(q), bytes) ||
+        overlaps(uw, need, reinterpret_cast<uintptr_t>(k), bytes) ||
+        overlaps(uw, need, reinterpret_cast<uintptr_t>(v), bytes) ||
+        overlaps(uw, need, reinterpret_cast<uintptr_t>(o), bytes) ||
+        (lse && overlaps(uw, need, reinterpret_cast<uintptr_t>(lse),
+                         static_cast<size_t>(B) * H * N * sizeof(float))))
+        return FA_ERR_INVALID_ARG;
+    const int bh = B * H;
+    CUtensorMap mq, mk, mv;
+    if ((s = prepare(q, k, v, bh, N, d, dtype, &mq, &mk, &mv)) != FA_OK)
+        return s;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    float *ws = static_cast<float *>(workspace);
+    if (dtype == FA_FP16) {
+        if (d == 64)
+            return causal ? launch_fa1<64, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
+                          : launch_fa1<64, false, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+        return causal ? launch_fa1<128, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
+                      : launch_fa1<128, false, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+    }
+    if (d == 64)
+        return causal ? launch_fa1<64, true, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
+                      : launch_fa1<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+    return causal ? launch_fa1<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
+                  : launch_fa1<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
 }
 
 fa_status_t fa_last_device_status(void *stream)

@@ -44,6 +44,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="base")
+    ap.add_argument("--kernel", choices=["fa2", "fa1"], default="fa2",
+                    help="fa2: the tiled FA2 forward (the product); fa1: the FA1-structured "
+                         "baseline the pages compare it against")
     ap.add_argument("--variants", default="noncausal,causal",
                     help="comma list of noncausal/causal launches per step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -80,10 +83,11 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def recorded_traffic(workload, src_hash):
+def recorded_traffic(workload, src_hash, kernel="fa2"):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, valid only while the kernel sources are the ones profiled."""
-    path = os.path.join(ROOT, "profiles", "fa_fwd_%s_dram.md" % workload)
+    stem = "fa_fwd" if kernel == "fa2" else "fa1_fwd"
+    path = os.path.join(ROOT, "profiles", "%s_%s_dram.md" % (stem, workload))
     try:
         text = open(path).read()
     except OSError:
@@ -288,6 +292,7 @@ def main():
               "l2": "flushed between timed steps (256 MiB write)",
               "parallelism": "dp%d (independent replicas)" % max(world, args.gpus)}
     step_flops = sum(flops_of(meta, c) for c in variants)
+    config["kernel"] = args.kernel
 
     if args.impl == "reference":
         return run_reference(args, q, k, v, meta, variants, config, step_flops, world, rank)
@@ -308,9 +313,16 @@ def main():
     stream = torch.cuda.current_stream(dev)
     scale = meta["d"] ** -0.5
 
+    if args.kernel == "fa1":
+        ws = torch.empty(fa.fa1_fwd_workspace_size(meta["B"], meta["H"], meta["N"], meta["d"]),
+                         dtype=torch.uint8, device=dev)
+        run = lambda q_, k_, v_, **kw: fa.fa1_fwd(q_, k_, v_, workspace=ws, **kw)
+    else:
+        run = fa.fa_fwd
+
     def step():
         for (o, lse), causal in zip(outs, variants):
-            fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
+            run(qd, kd, vd, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
 
     uuid = None
     try:
@@ -342,7 +354,7 @@ def main():
         flush.zero_()
         ev[i][0].record(stream)
         for j, ((o, lse), causal) in enumerate(zip(outs, variants)):
-            fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
+            run(qd, kd, vd, o=o, lse=lse, scale=scale, causal=causal, stream=stream)
             ev[i][j + 1].record(stream)
     torch.cuda.synchronize(dev)
     if dist is not None:
@@ -364,7 +376,7 @@ def main():
     # e2e through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(fa, torch, q, k, v, meta, variants, dev, stream, scale, step_flops,
+        e2e = run_e2e(run, torch, q, k, v, meta, variants, dev, stream, scale, step_flops,
                       max(3, min(K, 50)), dist)
 
     clocks = sampler.stop()
@@ -375,10 +387,11 @@ def main():
     achieved = flops_of(meta, dom_causal) / (dom_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     src_hash = kernel_source_hash()
-    traffic, traffic_src = recorded_traffic(args.workload, src_hash)
+    traffic, traffic_src = recorded_traffic(args.workload, src_hash, args.kernel)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "fa_fwd_kernel<%d,%s,%s>" % (meta["d"], "causal" if dom_causal else
+                "kernel": "%s_kernel<%d,%s,%s>" % ("fa_fwd" if args.kernel == "fa2" else "fa1_fwd",
+                                                   meta["d"], "causal" if dom_causal else
                                                        "noncausal", meta["dtype"]),
                 "peak_source": "%s bf16_tflops (burst; fp16 dense rate equals bf16)" % peak_src,
                 "launch_ms": dom_ms,
@@ -405,7 +418,7 @@ def main():
         dist.destroy_process_group()
 
 
-def run_e2e(fa, torch, q, k, v, meta, variants, dev, stream, scale, step_flops, steps, dist):
+def run_e2e(run, torch, q, k, v, meta, variants, dev, stream, scale, step_flops, steps, dist):
     hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
     qd, kd, vd = torch.empty_like(hq, device=dev), torch.empty_like(hk, device=dev), \
         torch.empty_like(hv, device=dev)
@@ -422,7 +435,7 @@ def run_e2e(fa, torch, q, k, v, meta, variants, dev, stream, scale, step_flops, 
         kd.copy_(hk, non_blocking=True)
         vd.copy_(hv, non_blocking=True)
         for (o, l), (ho, hl), causal in zip(douts, houts, variants):
-            fa.fa_fwd(qd, kd, vd, o=o, lse=l, scale=scale, causal=causal, stream=stream)
+            run(qd, kd, vd, o=o, lse=l, scale=scale, causal=causal, stream=stream)
             ho.copy_(o, non_blocking=True)
             hl.copy_(l, non_blocking=True)
 

@@ -28,6 +28,8 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -85,6 +87,36 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
 FA_API fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                    int B, int H, int N, int d, float scale, int causal,
                    fa_dtype_t dtype, void *stream);
+
+/*
+ * fa1_fwd_workspace_size -- bytes of device workspace fa1_fwd needs for a
+ * problem: B*H*N*(d+2) fp32 values (the running output, max and sum of every
+ * row).  0 for invalid sizes.
+ */
+FA_API size_t fa1_fwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa1_fwd -- the same attention forward computed with the FlashAttention-1
+ * loop nest that "Triton으로 FlashAttention 1·2 forward 구현하기" (sections
+ * "병렬화 단위", "출력 누적 방식") compares FA2 against: one CTA per (batch,
+ * head), K/V blocks in the outer loop, Q blocks inside; after each K/V block
+ * the normalised output and the statistics (m, l) of every row go to global
+ * memory in fp32 and come back for the next block.  A baseline for the FA2
+ * kernel above, not a faster path.
+ *
+ *  q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream: as for fa_fwd,
+ *            with the same checks and results (up to rounding order).
+ *  workspace: device pointer, 16-byte aligned, at least
+ *            fa1_fwd_workspace_size(B, H, N, d) bytes, not overlapping any
+ *            other buffer; owned by the caller; its contents on entry do not
+ *            matter and on return are scratch.  Calls that share a workspace
+ *            must not run concurrently.
+ * Errors: as fa_fwd, plus FA_ERR_INVALID_ARG for a missing, short or
+ * overlapping workspace and FA_ERR_MISALIGNED for a misaligned one.
+ */
+FA_API fa_status_t fa1_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                           void *workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                           float scale, int causal, fa_dtype_t dtype, void *stream);
 
 /*
  * fa_last_device_status -- synchronise `stream`, read and clear the device

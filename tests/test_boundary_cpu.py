@@ -74,6 +74,31 @@ def test_argument_checks(lib, kwargs, status):
     assert call(**kwargs) == status
 
 
+def test_fa1_workspace_size(lib):
+    assert fa.fa1_fwd_workspace_size(4, 32, 2048, 64) == 4 * 32 * 2048 * 66 * 4
+    assert fa.fa1_fwd_workspace_size(1, 1, 1, 128) == 130 * 4
+    assert fa.fa1_fwd_workspace_size(1, 1, 1, 96) == 0
+    assert fa.fa1_fwd_workspace_size(-1, 1, 1, 64) == 0
+
+
+W = 0x60000000
+
+
+def call_fa1(ws=W, ws_bytes=1 << 30, **kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=2, N=256, d=64, scale=0.125, causal=0, dtype=0)
+    a.update(kw)
+    return fa.fa1_fwd_raw(a["q"], a["k"], a["v"], a["o"], a["lse"], ws, ws_bytes, a["B"], a["H"],
+                          a["N"], a["d"], a["scale"], a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(ws=0), 1), (dict(ws_bytes=100), 1), (dict(ws=W + 8), 3), (dict(ws=Q), 1),
+    (dict(d=96), 2), (dict(causal=3), 1), (dict(N=0), 0),
+], ids=lambda x: str(x))
+def test_fa1_argument_checks(lib, kwargs, status):
+    assert call_fa1(**kwargs) == status
+
+
 def test_selftest_rejects_bad_limit_before_cuda(lib):
     assert fa.fa_selftest_wait_timeout(0) == 1
     assert fa.fa_selftest_wait_timeout(2_000_000) == 1
