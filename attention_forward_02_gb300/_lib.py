@@ -19,7 +19,7 @@ FA_FP16 = 0
 FA_BF16 = 1
 
 # every symbol include/fa.h declares
-EXPORTS = ("fa_fwd", "fa1_fwd_workspace_size", "fa1_fwd", "fa_last_device_status",
+EXPORTS = ("fa_fwd", "fa1_fwd_workspace_size", "fa1_fwd", "fa1_fwd_noalloc", "fa_last_device_status",
            "fa_selftest_wait_timeout", "fa_status_str", "fa_abi_version")
 
 _lib = None
@@ -55,6 +55,8 @@ def load(path=None):
     lib.fa1_fwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa1_fwd.restype = i
     lib.fa1_fwd.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i, i, vp]
+    lib.fa1_fwd_noalloc.restype = i
+    lib.fa1_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_last_device_status.restype = i
     lib.fa_last_device_status.argtypes = [vp]
     lib.fa_selftest_wait_timeout.restype = i

@@ -213,6 +213,29 @@ fa_status_t prepare(const void *q, const void *k, const void *v, int BH, int N, 
     return encode_qkv_map(st->encode, mv, v, BH, N, d, dtype);
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of fa1_fwd: its scratch lives in this fixed device
+// array instead of a caller workspace.  Every device that loads the library
+// holds the array until the process exits.
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
+static __device__ __align__(256) float g_fa1_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+struct NoAllocState {
+    std::once_flag once;
+    cudaError_t err = cudaErrorUnknown;
+    float *scratch = nullptr;  // device address of g_fa1_noalloc_scratch
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: look up the array's device
+// address (its name in host code is only a host-side stand-in).
+void init_noalloc(NoAllocState &st)
+{
+    void *ptr = nullptr;
+    st.err = cudaGetSymbolAddress(&ptr, g_fa1_noalloc_scratch);
+    st.scratch = (st.err == cudaSuccess) ? static_cast<float *>(ptr) : nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -278,6 +301,43 @@ fa_status_t fa1_fwd(const void *q, const void *k, const void *v, void *o, float 
         return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     float *ws = static_cast<float *>(workspace);
+    if (dtype == FA_FP16) {
+        if (d == 64)
+            return causal ? launch_fa1<64, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
+                          : launch_fa1<64, false, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+        return causal ? launch_fa1<128, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
+                      : launch_fa1<128, false, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+    }
+    if (d == 64)
+        return causal ? launch_fa1<64, true, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
+                      : launch_fa1<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+    return causal ? launch_fa1<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
+                  : launch_fa1<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+}
+
+fa_status_t fa1_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int H, int N, int d, float scale, int causal, fa_dtype_t dtype,
+                            void *stream)
+{
+    bool empty = false;
+    fa_status_t s = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
+    if (s != FA_OK || empty)
+        return s;
+    if (fa1_fwd_workspace_size(B, H, N, d) > kNoAllocScratchBytes)
+        return FA_ERR_UNSUPPORTED;  // problem needs more scratch than the fixed array holds
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FA_ERR_CUDA;
+    NoAllocState &na = g_noalloc[dev];
+    std::call_once(na.once, init_noalloc, std::ref(na));
+    if (na.err != cudaSuccess || na.scratch == nullptr)
+        return FA_ERR_CUDA;
+    const int bh = B * H;
+    CUtensorMap mq, mk, mv;
+    if ((s = prepare(q, k, v, bh, N, d, dtype, &mq, &mk, &mv)) != FA_OK)
+        return s;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    float *ws = na.scratch;
     if (dtype == FA_FP16) {
         if (d == 64)
             return causal ? launch_fa1<64, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)

@@ -119,6 +119,32 @@ FA_API fa_status_t fa1_fwd(const void *q, const void *k, const void *v, void *o,
                            float scale, int causal, fa_dtype_t dtype, void *stream);
 
 /*
+ * fa1_fwd_noalloc -- fa1_fwd without a workspace argument, for callers that
+ * cannot allocate device memory on their own: code running where cudaMalloc
+ * is unavailable or forbidden (a plugin or runtime that hands out only fixed
+ * input/output buffers, a latency path that must not call into the
+ * allocator).  The pages have no counterpart; this is a convenience of the
+ * library.
+ *
+ *  Arguments and results: as fa1_fwd, without workspace / workspace_bytes.
+ *  Scratch: a fixed 16 MiB device array inside the library, held by every
+ *            device that loads the library until the process exits.  Problems
+ *            needing more than that (fa1_fwd_workspace_size(B,H,N,d) > 16 MiB)
+ *            return FA_ERR_UNSUPPORTED before anything is launched.
+ *  No allocation: the call never calls cudaMalloc, cudaFree or any allocating
+ *            routine.  The first call on each device looks up the array's
+ *            device address (cudaGetSymbolAddress) with that device current;
+ *            make that first call before any stream capture.
+ *  Sharing: every call uses the same array and leaves its last contents in
+ *            it; the kernel writes each scratch value before reading it, so
+ *            nothing has to be cleared.  Calls that overlap on the GPU (other
+ *            streams, other threads) race on the array: serialise them.
+ */
+FA_API fa_status_t fa1_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int B, int H, int N, int d, float scale, int causal,
+                                   fa_dtype_t dtype, void *stream);
+
+/*
  * fa_last_device_status -- synchronise `stream`, read and clear the device
  * status word of the current device.  Returns FA_ERR_TIMEOUT if any kernel
  * launched since the last call gave up on a wait, FA_ERR_CUDA if the stream
