@@ -26,18 +26,15 @@ struct DeviceState {
     std::once_flag once;
     fa_status_t init_status = FA_ERR_CUDA;
     EncodeTiledFn encode = nullptr;
+    int num_sms = 0;
 };
 DeviceState g_dev[kMaxDevices];
-
-// Where P (the rounded softmax weights) lives between the two products.
-constexpr bool kPInTmem = true;
 
 template <int D, bool CAUSAL, typename T>
 cudaError_t set_smem_attr()
 {
-    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, T, kPInTmem>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                fa::KCfg<D, kPInTmem>::SMEM_ALLOC);
+    return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, T>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, fa::KCfg<D>::SMEM_ALLOC);
 }
 
 template <int D, bool CAUSAL, typename T>
@@ -60,6 +57,7 @@ void init_device(int dev, DeviceState &st)
         st.init_status = FA_ERR_UNSUPPORTED;
         return;
     }
+    st.num_sms = prop.multiProcessorCount;
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
@@ -121,17 +119,18 @@ fa_status_t encode_qkv_map(EncodeTiledFn encode, CUtensorMap *map, const void *p
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// Persistent launch: one CTA per SM (TMEM and shared memory allow one), each
+// walking its share of the (batch*head, 256-row Q block) work items.
 template <int D, bool CAUSAL, typename T>
 fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
-                   float *lse, int BH, int N, float scale, cudaStream_t stream)
+                   float *lse, int BH, int N, float scale, int num_sms, cudaStream_t stream)
 {
     const int num_q_blocks = (N + fa::kBM - 1) / fa::kBM;
+    const long long items = static_cast<long long>(BH) * num_q_blocks;
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    // one CTA per (Q block, batch*head), Q blocks of a head adjacent
-    const dim3 grid(static_cast<unsigned>(static_cast<long long>(BH) * num_q_blocks));
-    fa::fa_fwd_kernel<D, CAUSAL, T, kPInTmem>
-        <<<grid, fa::kNumThreads, fa::KCfg<D, kPInTmem>::SMEM_ALLOC, stream>>>(
-            mq, mk, mv, static_cast<T *>(o), lse, N, num_q_blocks, scale, scale_log2);
+    const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
+    fa::fa_fwd_kernel<D, CAUSAL, T><<<grid, fa::kNumThreads, fa::KCfg<D>::SMEM_ALLOC, stream>>>(
+        mq, mk, mv, static_cast<T *>(o), lse, N, BH, num_q_blocks, scale, scale_log2);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -202,12 +201,15 @@ fa_status_t check_args(const void *q, const void *k, const void *v, const void *
 
 // Device state plus the three TMA descriptors of Q, K, V.
 fa_status_t prepare(const void *q, const void *k, const void *v, int BH, int N, int d,
-                    fa_dtype_t dtype, CUtensorMap *mq, CUtensorMap *mk, CUtensorMap *mv)
+                    fa_dtype_t dtype, CUtensorMap *mq, CUtensorMap *mk, CUtensorMap *mv,
+                    int *num_sms = nullptr)
 {
     DeviceState *st = nullptr;
     fa_status_t s = device_state(&st);
     if (s != FA_OK)
         return s;
+    if (num_sms)
+        *num_sms = st->num_sms;
     if ((s = encode_qkv_map(st->encode, mq, q, BH, N, d, dtype)) != FA_OK) return s;
     if ((s = encode_qkv_map(st->encode, mk, k, BH, N, d, dtype)) != FA_OK) return s;
     return encode_qkv_map(st->encode, mv, v, BH, N, d, dtype);
@@ -249,21 +251,22 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
         return s;
     const int bh = B * H;
     CUtensorMap mq, mk, mv;
-    if ((s = prepare(q, k, v, bh, N, d, dtype, &mq, &mk, &mv)) != FA_OK)
+    int sms = 0;
+    if ((s = prepare(q, k, v, bh, N, d, dtype, &mq, &mk, &mv, &sms)) != FA_OK)
         return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (dtype == FA_FP16) {
         if (d == 64)
-            return causal ? launch<64, true, __half>(mq, mk, mv, o, lse, bh, N, scale, cs)
-                          : launch<64, false, __half>(mq, mk, mv, o, lse, bh, N, scale, cs);
-        return causal ? launch<128, true, __half>(mq, mk, mv, o, lse, bh, N, scale, cs)
-                      : launch<128, false, __half>(mq, mk, mv, o, lse, bh, N, scale, cs);
+            return causal ? launch<64, true, __half>(mq, mk, mv, o, lse, bh, N, scale, sms, cs)
+                          : launch<64, false, __half>(mq, mk, mv, o, lse, bh, N, scale, sms, cs);
+        return causal ? launch<128, true, __half>(mq, mk, mv, o, lse, bh, N, scale, sms, cs)
+                      : launch<128, false, __half>(mq, mk, mv, o, lse, bh, N, scale, sms, cs);
     }
     if (d == 64)
-        return causal ? launch<64, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs)
-                      : launch<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs);
-    return causal ? launch<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs)
-                  : launch<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, cs);
+        return causal ? launch<64, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, sms, cs)
+                      : launch<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, sms, cs);
+    return causal ? launch<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, sms, cs)
+                  : launch<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, sms, cs);
 }
 
 size_t fa1_fwd_workspace_size(int B, int H, int N, int d)

@@ -59,13 +59,13 @@ constexpr int kBN = 128;            // keys per K/V tile
 // warpgroup (warps 8 and 10 MMA issuers of sub-tiles 0 and 1, warp 9 TMA
 // producer, warp 11 idle).
 // Launched at 168 registers per thread (384 x 168 = 64512); the control
-// warpgroup drops to 80 and the softmax warpgroups rise to 208:
-// 256 x 208 + 128 x 80 = 63488 <= 64512.
+// warpgroup drops to 96 and the softmax warpgroups rise to 200:
+// 256 x 200 + 128 x 96 = 63488 <= 64512.
 constexpr int kNumThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-constexpr uint32_t kRegsSoftmax = 208;
-constexpr uint32_t kRegsControl = 80;
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsControl = 96;
 static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= 384 * 168, "register split");
 // TMEM columns: S0 @ 0, S1 @ 128, O0 @ 256, O1 @ 256 + D.  P_h (16-bit, two
 // per column) takes 64 columns: for D = 64 the spare columns 384 + 64 h, for
@@ -82,24 +82,30 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitLimitCycles = 1ll << 31;  // about one second at 2 GHz
 constexpr int kSwAtomBytes = 128 * 128;             // [128 rows x 64 cols] 16-bit swizzle block
 
-template <int D, bool P_TMEM>
+template <int D>
 struct KCfg {
     static constexpr int TILE = 128 * D * 2;  // bytes of one [128, D] 16-bit tile
-    static constexpr int SLOTS = P_TMEM ? (D == 64 ? 6 : 4) : (D == 64 ? 4 : 3);
-    static constexpr int Q_OFF = 0;           // Q0, Q1
-    static constexpr int KV_OFF = Q_OFF + 2 * TILE;
-    static constexpr int P_OFF = KV_OFF + SLOTS * TILE;  // P0, P1 (shared-memory variant)
-    static constexpr int P_TILE = 128 * kBN * 2;
-    static constexpr int BAR_OFF = P_OFF + (P_TMEM ? 0 : 2 * P_TILE);
-    static constexpr int B_QFULL = 0;
-    static constexpr int B_KVFULL = 1;
+    // D = 64: a 6-slot K/V ring and O staging tiles of their own, so the next
+    // item's Q can land while this item's output is stored.  D = 128: a 4-slot
+    // ring; O is staged in the sub-tile's Q tile, which the next item's Q then
+    // waits for (its items are long, so that wait matters little).
+    static constexpr bool STAGE_IN_Q = D == 128;
+    static constexpr int SLOTS = D == 64 ? 6 : 4;
+    static constexpr int Q_OFF = 0;                      // Q0, Q1
+    static constexpr int KV_OFF = Q_OFF + 2 * TILE;      // K/V ring
+    static constexpr int OST_OFF = STAGE_IN_Q ? Q_OFF : KV_OFF + SLOTS * TILE;  // O staging
+    static constexpr int BAR_OFF = KV_OFF + SLOTS * TILE + (STAGE_IN_Q ? 0 : 2 * TILE);
+    static constexpr int B_QFULL = 0;                    // two
+    static constexpr int B_QEMPTY = B_QFULL + 2;         // two
+    static constexpr int B_KVFULL = B_QEMPTY + 2;
     static constexpr int B_KVEMPTY = B_KVFULL + SLOTS;
     static constexpr int B_SFULL = B_KVEMPTY + SLOTS;  // two
     static constexpr int B_PFULL = B_SFULL + 2;        // two
     static constexpr int B_OFINAL = B_PFULL + 2;       // two
     static constexpr int B_SFREE = B_OFINAL + 2;       // two (early-S order only)
     static constexpr int B_OREADY = B_SFREE + 2;       // two (early-S order only)
-    static constexpr int B_DRAIN = B_OREADY + 2;       // two (one per MMA issuer)
+    static constexpr int B_OFREE = B_OREADY + 2;       // two
+    static constexpr int B_DRAIN = B_OFREE + 2;        // two (one per MMA issuer)
     static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // TMEM base address, abort flag
     static constexpr int SMEM_USED = SLOT_OFF + 16;
@@ -225,18 +231,45 @@ __device__ __forceinline__ float exp_tile(float (&s)[kBN], int limit, float c2, 
     return t.x + t.y;
 }
 
-template <int D, bool CAUSAL, typename T, bool P_TMEM>
+// Work item w (a 256-row Q block of one head) of a launch with BH heads and
+// nqb Q blocks per head.  Non-causal: head-major, so the CTAs working at the
+// same time share few heads' K/V in L2.  Causal: heaviest blocks (highest qb)
+// of every head first.
+template <bool CAUSAL>
+__device__ __forceinline__ void item_coords(int w, int BH, int nqb, int &bh, int &qb)
+{
+    if (CAUSAL) {
+        qb = nqb - 1 - w / BH;
+        bh = w % BH;
+    } else {
+        bh = w / nqb;
+        qb = w % nqb;
+    }
+}
+
+// The it-th work item of this CTA: round-robin over the grid; for causal
+// launches the direction alternates every round (heavy and light items even out).
+template <bool CAUSAL>
+__device__ __forceinline__ int item_of(int it)
+{
+    const int c = (CAUSAL && (it & 1)) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                                       : static_cast<int>(blockIdx.x);
+    return it * static_cast<int>(gridDim.x) + c;
+}
+
+template <int D, bool CAUSAL, typename T>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, T *__restrict__ out,
-                  float *__restrict__ lse, int N, int num_q_blocks, float scale, float scale_log2)
+                  float *__restrict__ lse, int N, int BH, int num_q_blocks, float scale,
+                  float scale_log2)
 {
-    using C = KCfg<D, P_TMEM>;
+    using C = KCfg<D>;
     // Early-S order (D = 64, where P has TMEM columns of its own): S_h,j+1 is
     // issued as soon as sub-tile h's softmax has finished with S_h,j, ahead of
     // P_h,j V_j, so the two softmax warpgroups need not wait for each other's
     // products.  With D = 128, P overwrites S_h, so S_h,j+1 follows P_h,j V_j.
-    constexpr bool EARLY_S = P_TMEM && D == 64;
+    constexpr bool EARLY_S = D == 64;
     constexpr int NUM_ISSUERS = EARLY_S ? 2 : 1;
     constexpr int SLOTS = C::SLOTS;
     constexpr int KSTEPS_QK = D / 16;  // UMMA_K = 16 for 16-bit operands
@@ -250,34 +283,35 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Q blocks of one head are adjacent in launch order (shared K/V stays in
-    // L2); within a head the heaviest causal blocks go first.
-    const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(num_q_blocks));
-    const int qb = num_q_blocks - 1 - static_cast<int>(blockIdx.x % static_cast<unsigned>(num_q_blocks));
-    const int row0 = qb * kBM;
+    const int num_items = BH * num_q_blocks;
     const int num_k_tiles = (N + kBN - 1) / kBN;
-    const int nk0 = CAUSAL ? min(2 * qb + 1, num_k_tiles) : num_k_tiles;  // sub-tile 0
-    const int nk1 = CAUSAL ? min(2 * qb + 2, num_k_tiles) : num_k_tiles;  // sub-tile 1 (>= nk0)
+    // key tiles of sub-tile h of Q block qb
+    auto nk_sub = [&](int qb, int h) {
+        return CAUSAL ? min(2 * qb + 1 + h, num_k_tiles) : num_k_tiles;
+    };
 
     auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + C::SLOT_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SLOT_OFF + 4);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_QFULL), 1);
         for (int s = 0; s < SLOTS; ++s) {
             mbar_init(bar(C::B_KVFULL + s), 1);
             mbar_init(bar(C::B_KVEMPTY + s), NUM_ISSUERS);  // one release per MMA issuer
         }
         for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(C::B_QFULL + h), 1);
+            // released by the products that read Q_h (one commit) and, when O
+            // is staged in Q_h, by the epilogue's stores (128 arrivals)
+            mbar_init(bar(C::B_QEMPTY + h), 1 + (C::STAGE_IN_Q ? 4 * 32 : 0));
             mbar_init(bar(C::B_SFULL + h), 1);
             mbar_init(bar(C::B_PFULL + h), 4 * 32);
             mbar_init(bar(C::B_OFINAL + h), 1);
             mbar_init(bar(C::B_SFREE + h), 4 * 32);
             mbar_init(bar(C::B_OREADY + h), 1);
+            mbar_init(bar(C::B_OFREE + h), 4 * 32);
+            mbar_init(bar(C::B_DRAIN + h), 1);
         }
-        mbar_init(bar(C::B_DRAIN + 0), 1);
-        mbar_init(bar(C::B_DRAIN + 1), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -293,35 +327,53 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (warp >= kMmaWarp) {
       reg_dealloc<kRegsControl>();
       if (warp == kTmaWarp && lane == 0) {
-            // ---------------- producer ----------------
+            // ---------------- producer: per work item Q0, Q1, then K_0, V_0, K_1, V_1, ... ----------------
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE);
-            for (int h = 0; h < 2; ++h)
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(sbase + C::Q_OFF + h * C::TILE + b * kSwAtomBytes, &tm_q,
-                                bar(C::B_QFULL), b * 64, row0 + h * kSubM, bh, pol_q);
-            int issued = 0;  // loads into the ring: K_j = load 2j, V_j = load 2j + 1
-            for (int L = 0; L < 2 * nk1; ++L) {
-                const int s = L % SLOTS;
-                if (L >= SLOTS && !wait_bounded(bar(C::B_KVEMPTY + s), ((L / SLOTS) - 1) & 1, abort_flag))
+            int L = 0;  // loads into the ring so far (all items)
+            int items = 0;
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int w = item_of<CAUSAL>(it);
+                if (w >= num_items)
                     break;
-                const CUtensorMap *map = (L & 1) ? &tm_v : &tm_k;
-                mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE);
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(sbase + C::KV_OFF + s * C::TILE + b * kSwAtomBytes, map,
-                                bar(C::B_KVFULL + s), b * 64, (L >> 1) * kBN, bh, pol_kv);
-                ++issued;
+                int bh, qb;
+                item_coords<CAUSAL>(w, BH, num_q_blocks, bh, qb);
+                for (int h = 0; ok && h < 2; ++h) {
+                    // Q_h of the previous item: every product that read it is done
+                    if (it > 0 && !(ok = wait_bounded(bar(C::B_QEMPTY + h), (it - 1) & 1, abort_flag)))
+                        break;
+                    mbar_arrive_expect_tx(bar(C::B_QFULL + h), C::TILE);
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(sbase + C::Q_OFF + h * C::TILE + b * kSwAtomBytes, &tm_q,
+                                    bar(C::B_QFULL + h), b * 64, qb * kBM + h * kSubM, bh, pol_q);
+                }
+                if (!ok)
+                    break;
+                ++items;
+                const int nloads = 2 * nk_sub(qb, 1);  // K_j = load 2j, V_j = load 2j + 1
+                for (int Ll = 0; Ll < nloads; ++Ll, ++L) {
+                    const int s = L % SLOTS;
+                    if (L >= SLOTS && !(ok = wait_bounded(bar(C::B_KVEMPTY + s), ((L / SLOTS) - 1) & 1, abort_flag)))
+                        break;
+                    const CUtensorMap *map = (Ll & 1) ? &tm_v : &tm_k;
+                    mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE);
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(sbase + C::KV_OFF + s * C::TILE + b * kSwAtomBytes, map,
+                                    bar(C::B_KVFULL + s), b * 64, (Ll >> 1) * kBN, bh, pol_kv);
+                }
             }
             // Wait for every copy this thread issued (immediate on the normal
             // path, where each one was consumed).
-            drain_bounded(bar(C::B_QFULL), 0);
+            for (int h = 0; h < 2; ++h)
+                if (items > 0)
+                    drain_bounded(bar(C::B_QFULL + h), (items - 1) & 1);
             for (int s = 0; s < SLOTS; ++s)
-                if (issued > s)
-                    drain_bounded(bar(C::B_KVFULL + s), ((issued - 1 - s) / SLOTS) & 1);
+                if (L > s)
+                    drain_bounded(bar(C::B_KVFULL + s), ((L - 1 - s) / SLOTS) & 1);
       } else if (lane == 0 && (warp == kMmaWarp || (NUM_ISSUERS == 2 && warp == kMmaWarp + 2))) {
             // ---------------- MMA issuer(s) ----------------
             // A thread that issues tcgen05.mma is held for about the product's
@@ -335,7 +387,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int me = (warp == kMmaWarp) ? 0 : 1;
             const int h_lo = NUM_ISSUERS == 2 ? me : 0;
             const int h_hi = NUM_ISSUERS == 2 ? me + 1 : 2;
-            const int nk_mine = NUM_ISSUERS == 2 ? (me == 0 ? nk0 : nk1) : nk1;
             constexpr uint32_t idesc_s = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, kBN, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, D, false, true);
             auto slot_of = [](int L) { return L % SLOTS; };
@@ -346,9 +397,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const uint64_t desc_k0 = make_sdesc_sw128(sbase + C::KV_OFF, 16, 1024);
             const uint64_t desc_v0 = make_sdesc_sw128(sbase + C::KV_OFF, kSwAtomBytes, 1024);
             const uint64_t desc_q0 = make_sdesc_sw128(sbase + C::Q_OFF, 16, 1024);
-            auto nk_of = [&](int h) { return h == 0 ? nk0 : nk1; };
+            int Lb = 0;              // ring index of the current item's K_0
+            // key tiles of sub-tile 0 / 1 in earlier items (scalars, not an
+            // array: a runtime-indexed array would live in local memory)
+            int done0 = 0, done1 = 0;
             auto issue_s = [&](int h, int j) {
-                const uint64_t kd = desc_k0 + static_cast<uint32_t>((slot_of(2 * j) * C::TILE) >> 4);
+                const uint64_t kd = desc_k0 + static_cast<uint32_t>((slot_of(Lb + 2 * j) * C::TILE) >> 4);
                 const uint64_t qd = desc_q0 + static_cast<uint32_t>((h * C::TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_QK; ++kk) {
@@ -357,115 +411,142 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             };
             auto issue_pv = [&](int h, int j) {
-                const uint64_t vd = desc_v0 + static_cast<uint32_t>((slot_of(2 * j + 1) * C::TILE) >> 4);
+                const uint64_t vd = desc_v0 + static_cast<uint32_t>((slot_of(Lb + 2 * j + 1) * C::TILE) >> 4);
                 const uint32_t d_o = tmem + kTmemO + h * D;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_PV; ++kk) {
                     // V: MN-major; 16 key rows (2048 B) per K step; the two
                     // 64-column blocks of D = 128 are kSwAtomBytes apart.
-                    const uint64_t bd = vd + static_cast<uint32_t>((kk * 2048) >> 4);
-                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                    if constexpr (P_TMEM) {
-                        // P_h,j: 16-bit, packed two per column; 8 columns per K step
-                        umma_f16_ts(d_o, tmem + tmem_p_col<D>(h) + kk * 8, bd, idesc_o, acc);
-                    } else {
-                        const uint32_t pt = sbase + C::P_OFF + h * C::P_TILE;
-                        const uint32_t poff = (kk >> 2) * kSwAtomBytes + (kk & 3) * 32;
-                        umma_f16_ss(d_o, make_sdesc_sw128(pt + poff, 16, 1024), bd, idesc_o, acc);
-                    }
+                    // P_h,j: 16-bit in TMEM, two per column; 8 columns per K step.
+                    umma_f16_ts(d_o, tmem + tmem_p_col<D>(h) + kk * 8,
+                                vd + static_cast<uint32_t>((kk * 2048) >> 4), idesc_o,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
-            auto wait_load = [&](int L) {
-                return wait_bounded(bar(C::B_KVFULL + slot_of(L)), par_of(L), abort_flag);
+            auto wait_load = [&](int l) {
+                return wait_bounded(bar(C::B_KVFULL + slot_of(Lb + l)), par_of(Lb + l), abort_flag);
             };
-            // Releases load L: after this issuer's products that read it
-            // (commit), or, when none did, as soon as it has landed.
-            auto release = [&](int L, bool used) -> bool {
+            // Releases load l of this item: after this issuer's products that
+            // read it (commit), or, when none did, as soon as it has landed.
+            auto release = [&](int l, bool used) -> bool {
                 if (used) {
-                    umma_commit(bar(C::B_KVEMPTY + slot_of(L)));
+                    umma_commit(bar(C::B_KVEMPTY + slot_of(Lb + l)));
                     return true;
                 }
-                if (!wait_load(L))
+                if (!wait_load(l))
                     return false;
-                mbar_arrive(bar(C::B_KVEMPTY + slot_of(L)));
+                mbar_arrive(bar(C::B_KVEMPTY + slot_of(Lb + l)));
                 return true;
             };
-            bool ok = wait_bounded(bar(C::B_QFULL), 0, abort_flag) && wait_load(0);
-            if (ok) {
+            // the first P V product of an item overwrites O_h: the previous
+            // item's epilogue must have read it
+            auto o_free = [&](int h, int it) {
+                return it == 0 || wait_bounded(bar(C::B_OFREE + h), (it - 1) & 1, abort_flag);
+            };
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int w = item_of<CAUSAL>(it);
+                if (w >= num_items)
+                    break;
+                int bh, qb;
+                item_coords<CAUSAL>(w, BH, num_q_blocks, bh, qb);
+                (void)bh;
+                const int nk0 = nk_sub(qb, 0), nk1 = nk_sub(qb, 1);
+                auto nk_of = [&](int h) { return h == 0 ? nk0 : nk1; };
+                auto done_of = [&](int h) { return h == 0 ? done0 : done1; };
+                for (int h = h_lo; ok && h < h_hi; ++h) {
+                    ok = wait_bounded(bar(C::B_QFULL + h), it & 1, abort_flag);
+                    // early-S: S_h,0 overwrites S_h, which the previous item's
+                    // last softmax step must have finished reading
+                    if (ok && EARLY_S && it > 0)
+                        ok = wait_bounded(bar(C::B_SFREE + h), (done_of(h) - 1) & 1, abort_flag);
+                }
+                ok = ok && wait_load(0);
+                if (!ok)
+                    break;
                 tc_fence_after();
                 for (int h = h_lo; h < h_hi; ++h) {
                     issue_s(h, 0);
                     umma_commit(bar(C::B_SFULL + h));
                 }
                 release(0, true);
-            }
-            for (int j = 0; ok && j < nk1; ++j) {
-                if constexpr (EARLY_S) {
-                    // next S products first, then this tile's P V products
-                    bool k_used = false;
-                    for (int h = h_lo; ok && h < h_hi; ++h) {
-                        if (j + 1 >= nk_of(h))
-                            continue;
-                        ok = wait_bounded(bar(C::B_SFREE + h), j & 1, abort_flag) &&
-                             (k_used || wait_load(2 * j + 2));
-                        if (!ok)
-                            break;
-                        tc_fence_after();
-                        issue_s(h, j + 1);
-                        umma_commit(bar(C::B_SFULL + h));
-                        k_used = true;
-                    }
-                    if (ok && j + 1 < nk1)
-                        ok = release(2 * j + 2, k_used);
-                    bool v_used = false;
-                    for (int h = h_lo; ok && h < h_hi; ++h) {
-                        if (j >= nk_of(h))
-                            continue;
-                        ok = (v_used || wait_load(2 * j + 1)) &&
-                             wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
-                        if (!ok)
-                            break;
-                        tc_fence_after();
-                        issue_pv(h, j);
-                        umma_commit(bar(C::B_OREADY + h));
-                        if (j + 1 == nk_of(h))
-                            umma_commit(bar(C::B_OFINAL + h));
-                        v_used = true;
-                    }
-                    if (ok)
-                        ok = release(2 * j + 1, v_used);
-                } else {
-                    // per sub-tile: P V of this tile, then the next S product
-                    bool v_used = false, k_used = false;
-                    for (int h = h_lo; ok && h < h_hi; ++h) {
-                        if (j >= nk_of(h))
-                            continue;
-                        ok = (v_used || wait_load(2 * j + 1)) &&
-                             wait_bounded(bar(C::B_PFULL + h), j & 1, abort_flag);
-                        if (!ok)
-                            break;
-                        tc_fence_after();
-                        issue_pv(h, j);
-                        v_used = true;
-                        if (j + 1 < nk_of(h)) {
-                            ok = k_used || wait_load(2 * j + 2);
+                for (int j = 0; ok && j < nk1; ++j) {
+                    if constexpr (EARLY_S) {
+                        // next S products first, then this tile's P V products
+                        bool k_used = false;
+                        for (int h = h_lo; ok && h < h_hi; ++h) {
+                            if (j + 1 >= nk_of(h))
+                                continue;
+                            ok = wait_bounded(bar(C::B_SFREE + h), (done_of(h) + j) & 1, abort_flag) &&
+                                 (k_used || wait_load(2 * j + 2));
                             if (!ok)
                                 break;
                             tc_fence_after();
                             issue_s(h, j + 1);
                             umma_commit(bar(C::B_SFULL + h));
                             k_used = true;
-                        } else {
-                            umma_commit(bar(C::B_OFINAL + h));
                         }
+                        if (ok && j + 1 < nk1)
+                            ok = release(2 * j + 2, k_used);
+                        bool v_used = false;
+                        for (int h = h_lo; ok && h < h_hi; ++h) {
+                            if (j >= nk_of(h))
+                                continue;
+                            ok = (v_used || wait_load(2 * j + 1)) &&
+                                 wait_bounded(bar(C::B_PFULL + h), (done_of(h) + j) & 1, abort_flag) &&
+                                 (j > 0 || o_free(h, it));
+                            if (!ok)
+                                break;
+                            tc_fence_after();
+                            issue_pv(h, j);
+                            umma_commit(bar(C::B_OREADY + h));
+                            if (j + 1 == nk_of(h))
+                                umma_commit(bar(C::B_OFINAL + h));
+                            v_used = true;
+                        }
+                        if (ok)
+                            ok = release(2 * j + 1, v_used);
+                    } else {
+                        // per sub-tile: P V of this tile, then the next S product
+                        bool v_used = false, k_used = false;
+                        for (int h = h_lo; ok && h < h_hi; ++h) {
+                            if (j >= nk_of(h))
+                                continue;
+                            ok = (v_used || wait_load(2 * j + 1)) &&
+                                 wait_bounded(bar(C::B_PFULL + h), (done_of(h) + j) & 1, abort_flag) &&
+                                 (j > 0 || o_free(h, it));
+                            if (!ok)
+                                break;
+                            tc_fence_after();
+                            issue_pv(h, j);
+                            v_used = true;
+                            if (j + 1 < nk_of(h)) {
+                                ok = k_used || wait_load(2 * j + 2);
+                                if (!ok)
+                                    break;
+                                tc_fence_after();
+                                issue_s(h, j + 1);
+                                umma_commit(bar(C::B_SFULL + h));
+                                k_used = true;
+                            } else {
+                                umma_commit(bar(C::B_OFINAL + h));
+                            }
+                        }
+                        if (ok)
+                            ok = release(2 * j + 1, v_used);
+                        if (ok && j + 1 < nk1)
+                            ok = release(2 * j + 2, k_used);
                     }
-                    if (ok)
-                        ok = release(2 * j + 1, v_used);
-                    if (ok && j + 1 < nk1)
-                        ok = release(2 * j + 2, k_used);
                 }
+                if (!ok)
+                    break;
+                // every product reading Q_h of this item has been issued
+                for (int h = h_lo; h < h_hi; ++h)
+                    umma_commit(bar(C::B_QEMPTY + h));
+                done0 += nk0;
+                done1 += nk1;
+                Lb += 2 * nk1;
             }
-            (void)nk_mine;
             // every MMA this thread issued has completed once this arrives
             umma_commit(bar(C::B_DRAIN + me));
             drain_bounded(bar(C::B_DRAIN + me), 0);
@@ -475,167 +556,170 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // ---------------- softmax warpgroup h (warps 4h .. 4h+3) ----------------
         const int h = warp >> 2;
         const int r = threadIdx.x & 127;  // row within the sub-tile == TMEM lane
-        const int qrow = row0 + h * kSubM + r;
-        const int nkh = h == 0 ? nk0 : nk1;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(h * kBN);
         const uint32_t o_tm = tmem + lane_base + kTmemO + static_cast<uint32_t>(h * D);
         const uint32_t p_tm = tmem + lane_base + tmem_p_col<D>(h);
-        float m_ref = -INFINITY;  // reference max (raw score units; scale >= 0)
-        float l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < nkh; ++j) {
-            ok = wait_bounded(bar(C::B_SFULL + h), j & 1, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok)
+        const uint32_t stage = sbase + C::OST_OFF + h * C::TILE;
+        int done = 0;  // key tiles of this sub-tile in earlier items
+        for (int it = 0;; ++it) {
+            const int w = item_of<CAUSAL>(it);
+            if (w >= num_items)
                 break;
-            tc_fence_after();
-            float s[kBN];
-            tmem_ld128(s_tm, s);
-            // keys [kbase, kbase + limit) are allowed for this row (limit >= 1)
-            const int kbase = j * kBN;
-            int limit = min(kBN, N - kbase);
-            if (CAUSAL)
-                limit = min(limit, qrow - kbase + 1);
-            const bool masked = __any_sync(0xffffffffu, limit < kBN);
-            if (masked)
-                mask_tail(s, limit);
-            // Tile 0 sets the reference max from its own row max.  Later tiles
-            // exponentiate against the current reference while their row max
-            // is taken; only a row max that outgrows the reference by more than
-            // kRescaleLog2 (rare) sends the warp down the redo path.
-            float alpha = 1.f;
-            float rsum;
-            if (j == 0) {
-                m_ref = row_max(s);
-                alpha = 0.f;
-                rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
-                              : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
-            } else {
-                const float mt = row_max(s);
-                rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
-                              : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
-                const bool grow = (mt - m_ref) * scale_log2 > kRescaleLog2;
-                if (__any_sync(0xffffffffu, grow)) {
-                    if (grow) {
-                        alpha = ex2_approx((m_ref - mt) * scale_log2);
-                        m_ref = mt;
-                    }
-                    // S_h is intact until P_h is written below: redo the tile
-                    tmem_ld128(s_tm, s);
-                    if (masked)
-                        mask_tail(s, limit);
+            int bh, qb;
+            item_coords<CAUSAL>(w, BH, num_q_blocks, bh, qb);
+            const int row0 = qb * kBM + h * kSubM;
+            const int qrow = row0 + r;
+            const int nkh = nk_sub(qb, h);
+            float m_ref = -INFINITY;  // reference max (raw score units; scale >= 0)
+            float l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nkh; ++j) {
+                const uint32_t ph = static_cast<uint32_t>((done + j) & 1);
+                ok = wait_bounded(bar(C::B_SFULL + h), ph, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                float s[kBN];
+                tmem_ld128(s_tm, s);
+                // keys [kbase, kbase + limit) are allowed for this row (limit >= 1)
+                const int kbase = j * kBN;
+                int limit = min(kBN, N - kbase);
+                if (CAUSAL)
+                    limit = min(limit, qrow - kbase + 1);
+                const bool masked = __any_sync(0xffffffffu, limit < kBN);
+                if (masked)
+                    mask_tail(s, limit);
+                // Tile 0 sets the reference max from its own row max.  Later tiles
+                // exponentiate against the current reference while their row max
+                // is taken; only a row max that outgrows the reference by more
+                // than kRescaleLog2 (rare) sends the warp down the redo path.
+                float alpha = 1.f;
+                float rsum;
+                if (j == 0) {
+                    m_ref = row_max(s);
+                    alpha = 0.f;
                     rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
                                   : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
+                } else {
+                    const float mt = row_max(s);
+                    rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                                  : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
+                    const bool grow = (mt - m_ref) * scale_log2 > kRescaleLog2;
+                    if (__any_sync(0xffffffffu, grow)) {
+                        if (grow) {
+                            alpha = ex2_approx((m_ref - mt) * scale_log2);
+                            m_ref = mt;
+                        }
+                        // S_h is intact until P_h is written below: redo the tile
+                        tmem_ld128(s_tm, s);
+                        if (masked)
+                            mask_tail(s, limit);
+                        rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                                      : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
+                    }
                 }
-            }
-            l = l * alpha + rsum;
-            if constexpr (EARLY_S) {
-                // S_h,j is no longer needed: let the next S_h product in
+                l = l * alpha + rsum;
+                if constexpr (EARLY_S) {
+                    // S_h,j is no longer needed: let the next S_h product in
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_SFREE + h));
+                    // P_h,j-1 V_{j-1} must have read P_h before it is overwritten
+                    // (and O_h must be complete before a rescale below).  For
+                    // j = 0 the previous item's last product has completed: this
+                    // warpgroup waited for it before its epilogue.
+                    if (j > 0) {
+                        ok = wait_bounded(bar(C::B_OREADY + h), ph ^ 1u, abort_flag);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                    }
+                }
+                // P_h,j rounded to the input dtype
+                {
+                    uint32_t pw[64];
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        pw[c] = DTypeTraits<T>::pack(s[2 * c], s[2 * c + 1]);
+                    tmem_st64(p_tm, pw);
+                }
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    // O_h must hold P V up to tile j-1, and P_h,j V_j is not issued
+                    // before this warpgroup arrives below.  In the early-S order
+                    // that product was awaited above; in the other order the S_h,j
+                    // product, issued after it, has completed.
+#pragma unroll
+                    for (int c4 = 0; c4 < D / 32; ++c4) {
+                        uint32_t u[32];
+                        tmem_ld32(o_tm + c4 * 32, u);
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float2 v = fmul2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
+                                                   make_float2(alpha, alpha));
+                            u[c] = __float_as_uint(v.x);
+                            u[c + 1] = __float_as_uint(v.y);
+                        }
+                        tmem_st32(o_tm + c4 * 32, u);
+                    }
+                }
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(C::B_SFREE + h));
+                mbar_arrive(bar(C::B_PFULL + h));
             }
 
-            if constexpr (EARLY_S) {
-                // P_h,j-1 V_{j-1} must have read P_h before it is overwritten
-                // (and O_h must be complete before a rescale below).
-                if (j > 0) {
-                    ok = wait_bounded(bar(C::B_OREADY + h), (j - 1) & 1, abort_flag);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                }
+            // ---------------- epilogue of sub-tile h ----------------
+            // Both named barriers below are reached by all four warps, whatever
+            // happened; their OR-reductions give every warp the same decision.
+            if (ok) {
+                ok = wait_bounded(bar(C::B_OFINAL + h), it & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
             }
-
-            // P_h,j rounded to the input dtype
-            if constexpr (P_TMEM) {
-                uint32_t w[64];
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    w[c] = DTypeTraits<T>::pack(s[2 * c], s[2 * c + 1]);
-                tmem_st64(p_tm, w);
-            } else {
-                const uint32_t pt = sbase + C::P_OFF + h * C::P_TILE;
-#pragma unroll
-                for (int ch = 0; ch < kBN / 8; ++ch) {
-                    const uint32_t w0 = DTypeTraits<T>::pack(s[ch * 8 + 0], s[ch * 8 + 1]);
-                    const uint32_t w1 = DTypeTraits<T>::pack(s[ch * 8 + 2], s[ch * 8 + 3]);
-                    const uint32_t w2 = DTypeTraits<T>::pack(s[ch * 8 + 4], s[ch * 8 + 5]);
-                    const uint32_t w3 = DTypeTraits<T>::pack(s[ch * 8 + 6], s[ch * 8 + 7]);
-                    st_shared_v4(pt + sw128_offset(r, ch), w0, w1, w2, w3);
-                }
-                fence_proxy_async_smem();
-            }
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O_h must hold P V up to tile j-1, and P_h,j V_j is not issued
-                // before this warpgroup arrives below.  In the early-S order
-                // that product was awaited above; in the other order the S_h,j
-                // product, issued after it, has completed.
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = 1.f / l;
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
                     uint32_t u[32];
                     tmem_ld32(o_tm + c4 * 32, u);
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const float2 v = fmul2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])),
-                                               make_float2(alpha, alpha));
-                        u[c] = __float_as_uint(v.x);
-                        u[c + 1] = __float_as_uint(v.y);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float *f = reinterpret_cast<const float *>(u) + q4 * 8;
+                        st_shared_v4(stage + sw128_offset(r, c4 * 4 + q4),
+                                     DTypeTraits<T>::pack(f[0] * inv_l, f[1] * inv_l),
+                                     DTypeTraits<T>::pack(f[2] * inv_l, f[3] * inv_l),
+                                     DTypeTraits<T>::pack(f[4] * inv_l, f[5] * inv_l),
+                                     DTypeTraits<T>::pack(f[6] * inv_l, f[7] * inv_l));
                     }
-                    tmem_st32(o_tm + c4 * 32, u);
                 }
+                // O_h has been read: the next item's first P V product may overwrite it
+                tc_fence_before();
+                mbar_arrive(bar(C::B_OFREE + h));
+                if (lse != nullptr && qrow < N)
+                    lse[static_cast<size_t>(bh) * N + qrow] = m_ref * scale + logf(l);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL + h));
-        }
-
-        // ---------------- epilogue of sub-tile h ----------------
-        // Every thread of the warpgroup reaches the named barrier; a warp that
-        // gave up has set the abort flag first, so after the barrier the four
-        // warps agree on whether the staged tile is whole.
-        if (ok) {
-            ok = wait_bounded(bar(C::B_OFINAL + h), 0, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        // Q_h is dead: every product that read it has completed.
-        const uint32_t stage = sbase + C::Q_OFF + h * C::TILE;
-        if (ok) {
-            tc_fence_after();
-            const float inv_l = 1.f / l;
-#pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-                uint32_t u[32];
-                tmem_ld32(o_tm + c4 * 32, u);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const float *f = reinterpret_cast<const float *>(u) + q4 * 8;
-                    st_shared_v4(stage + sw128_offset(r, c4 * 4 + q4),
-                                 DTypeTraits<T>::pack(f[0] * inv_l, f[1] * inv_l),
-                                 DTypeTraits<T>::pack(f[2] * inv_l, f[3] * inv_l),
-                                 DTypeTraits<T>::pack(f[4] * inv_l, f[5] * inv_l),
-                                 DTypeTraits<T>::pack(f[6] * inv_l, f[7] * inv_l));
-                }
-            }
-            if (lse != nullptr && qrow < N)
-                lse[static_cast<size_t>(bh) * N + qrow] = m_ref * scale + logf(l);
-        }
-        named_bar_sync(1 + h, 4 * 32);
-        if (*abort_flag == 0) {
-            constexpr int CHUNKS_PER_ROW = D / 8;
-            const int srow0 = row0 + h * kSubM;
-            uint8_t *obase = reinterpret_cast<uint8_t *>(out) +
-                             (static_cast<size_t>(bh) * N + srow0) * D * sizeof(T);
+            const bool bad = named_bar_or(1 + h, 4 * 32, !ok || *abort_flag != 0);
+            if (!bad) {
+                constexpr int CHUNKS_PER_ROW = D / 8;
+                uint8_t *obase = reinterpret_cast<uint8_t *>(out) +
+                                 (static_cast<size_t>(bh) * N + row0) * D * sizeof(T);
 #pragma unroll 4
-            for (int idx = r; idx < kSubM * CHUNKS_PER_ROW; idx += 4 * 32) {
-                const int row = idx / CHUNKS_PER_ROW;
-                const int ch = idx % CHUNKS_PER_ROW;
-                const uint4 val = ld_shared_v4(stage + sw128_offset(row, ch));
-                if (srow0 + row < N)
-                    *reinterpret_cast<uint4 *>(obase + (static_cast<size_t>(row) * D + ch * 8) *
-                                                           sizeof(T)) = val;
+                for (int idx = r; idx < kSubM * CHUNKS_PER_ROW; idx += 4 * 32) {
+                    const int row = idx / CHUNKS_PER_ROW;
+                    const int ch = idx % CHUNKS_PER_ROW;
+                    const uint4 val = ld_shared_v4(stage + sw128_offset(row, ch));
+                    if (row0 + row < N)
+                        *reinterpret_cast<uint4 *>(obase + (static_cast<size_t>(row) * D + ch * 8) *
+                                                               sizeof(T)) = val;
+                }
             }
+            // the staging tile is free again; stop together if anything failed
+            if constexpr (C::STAGE_IN_Q)
+                mbar_arrive(bar(C::B_QEMPTY + h));  // the next item's Q_h may land
+            if (named_bar_or(1 + h, 4 * 32, bad || *abort_flag != 0))
+                break;
+            done += nkh;
         }
         tc_fence_before();
     }

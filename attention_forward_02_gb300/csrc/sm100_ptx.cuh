@@ -103,6 +103,22 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Named barrier that also ORs a predicate across the participating threads:
+// every thread gets the same result.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // Named barrier over a subset of the CTA's warps.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
