@@ -57,6 +57,10 @@ class Oracle:
         L.oracle_online_row.restype = ctypes.c_int
         L.oracle_online_row.argtypes = [_dp, _dp, ctypes.c_long, ctypes.c_long, _lp, _lp,
                                         ctypes.c_long, _dp, _dp, _dp, _dp]
+        L.oracle_attention_bwd.restype = ctypes.c_int
+        L.oracle_attention_bwd.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                           ctypes.c_long, ctypes.c_double, ctypes.c_int,
+                                           _dp, _dp, _dp, ctypes.c_int]
         L.oracle_abi_version.restype = ctypes.c_int
 
     # -- helpers -----------------------------------------------------------
@@ -123,6 +127,23 @@ class Oracle:
         if st != 0:
             raise OracleError("oracle_scores_row returned %d" % st)
         return s[: n.value].copy()
+
+    def attention_bwd(self, q, k, v, g, scale, causal=False, threads=None):
+        """Gradients (dq, dk, dv) of sum(o * g) for the plain definition.
+
+        q, k, v, g: [B, H, N, d]; returns three fp64 arrays of that shape."""
+        q, k, v, g = self._f64(q), self._f64(k), self._f64(v), self._f64(g)
+        if q.ndim != 4 or any(t.shape != q.shape for t in (k, v, g)):
+            raise OracleError("q, k, v, g must share a [B,H,N,d] shape")
+        B, H, N, d = q.shape
+        dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+        st = self._lib.oracle_attention_bwd(self._ptr(q), self._ptr(k), self._ptr(v),
+                                            self._ptr(g), B * H, N, d, float(scale),
+                                            int(bool(causal)), self._ptr(dq), self._ptr(dk),
+                                            self._ptr(dv), threads or self.default_threads())
+        if st != 0:
+            raise OracleError("oracle_attention_bwd returned %d" % st)
+        return dq, dk, dv
 
     # -- online recurrence -------------------------------------------------
     def online_row(self, s, v, blocks):

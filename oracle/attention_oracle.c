@@ -38,8 +38,11 @@
  *    tests can check the page's hand-worked intermediate values
  *    (section 3.6.5) and the block-order independence the page claims.
  *
+ *  - oracle_attention_bwd: the gradients of the plain definition (softmax
+ *    Jacobian), for the backward pass.
+ *
  * Every function here is pinned by tests under tests/ (worked example,
- * exercise, closed forms, invariants, source mutations).
+ * exercise, closed forms, invariants, finite differences, source mutations).
  *
  * Arithmetic: IEEE fp64, evaluated in source order (built without
  * fast-math, so the compiler does not reassociate the sums).
@@ -348,6 +351,150 @@ int oracle_online_row(const double *s, const double *v, long n, long d,
     free(seen);
     free(acc);
     return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Backward pass: gradients of the plain definition.                    */
+/*
+ * For one head with scores s_ij = scale * <q_i, k_j> over the allowed keys,
+ * p_ij = softmax_j(s_ij) and o_i = sum_j p_ij v_j, and an upstream gradient
+ * g_i = dL/do_i, the chain rule through the row softmax gives
+ *     dv_j  = sum_i p_ij g_i
+ *     dp_ij = <g_i, v_j>
+ *     ds_ij = p_ij * (dp_ij - sum_k p_ik dp_ik)          (softmax Jacobian)
+ *     dq_i  = scale * sum_j ds_ij k_j
+ *     dk_j  = scale * sum_i ds_ij q_i
+ * "3.6 어텐션 I", section 3.6.7, describes the backward as recomputing S and P
+ * from Q, K and the saved row statistics; this is the quantity it computes.
+ * Rows are processed one at a time (two passes over the keys, like the
+ * forward), so memory is O(N d) per head.
+ */
+static void backward_head(const double *q, const double *k, const double *v, const double *g,
+                          long n, long d, double scale, int causal, double *s, double *dp,
+                          double *dq, double *dk, double *dv)
+{
+    for (long x = 0; x < n * d; ++x) {
+        dq[x] = 0.0;
+        dk[x] = 0.0;
+        dv[x] = 0.0;
+    }
+    for (long i = 0; i < n; ++i) {
+        long n_keys = allowed_keys(i, n, causal);
+        scores_row(q, k, i, n_keys, d, scale, s);
+        double m = -INFINITY;
+        for (long j = 0; j < n_keys; ++j)
+            if (s[j] > m)
+                m = s[j];
+        double row_sum = 0.0;
+        for (long j = 0; j < n_keys; ++j)
+            row_sum += exp(s[j] - m);
+        /* s <- p_ij, dp <- <g_i, v_j> */
+        double pdp = 0.0;
+        for (long j = 0; j < n_keys; ++j) {
+            s[j] = exp(s[j] - m) / row_sum;
+            double dot = 0.0;
+            for (long c = 0; c < d; ++c)
+                dot += g[i * d + c] * v[j * d + c];
+            dp[j] = dot;
+            pdp += s[j] * dot;
+        }
+        for (long j = 0; j < n_keys; ++j) {
+            double ds = s[j] * (dp[j] - pdp);
+            for (long c = 0; c < d; ++c) {
+                dv[j * d + c] += s[j] * g[i * d + c];
+                dq[i * d + c] += scale * ds * k[j * d + c];
+                dk[j * d + c] += scale * ds * q[i * d + c];
+            }
+        }
+    }
+}
+
+typedef struct {
+    const double *q, *k, *v, *g;
+    long n, d;
+    double scale;
+    int causal;
+    double *dq, *dk, *dv;
+    long begin, end;
+    int status;
+} head_job;
+
+static void *head_worker(void *arg)
+{
+    head_job *job = (head_job *)arg;
+    double *s = (double *)malloc((size_t)(job->n > 0 ? job->n : 1) * sizeof(double));
+    double *dp = (double *)malloc((size_t)(job->n > 0 ? job->n : 1) * sizeof(double));
+    if (!s || !dp) {
+        free(s);
+        free(dp);
+        job->status = ORACLE_ENOMEM;
+        return NULL;
+    }
+    long he = job->n * job->d;
+    for (long bh = job->begin; bh < job->end; ++bh)
+        backward_head(job->q + bh * he, job->k + bh * he, job->v + bh * he, job->g + bh * he,
+                      job->n, job->d, job->scale, job->causal, s, dp, job->dq + bh * he,
+                      job->dk + bh * he, job->dv + bh * he);
+    free(s);
+    free(dp);
+    job->status = ORACLE_OK;
+    return NULL;
+}
+
+/*
+ * oracle_attention_bwd: gradients dq, dk, dv ([BH, N, d] fp64) of
+ * L = sum(o * g) for the plain definition, given q, k, v and g = dL/do
+ * ([BH, N, d] fp64).  Threads split the heads.
+ */
+int oracle_attention_bwd(const double *q, const double *k, const double *v, const double *g,
+                         long BH, long N, long d, double scale, int causal, double *dq,
+                         double *dk, double *dv, int nthreads)
+{
+    if (BH < 0 || N < 0 || d < 1 || (causal != 0 && causal != 1))
+        return ORACLE_EINVAL;
+    if (BH == 0 || N == 0)
+        return ORACLE_OK;
+    if (!q || !k || !v || !g || !dq || !dk || !dv)
+        return ORACLE_EINVAL;
+    if (nthreads <= 0)
+        nthreads = 1;
+    if (nthreads > BH)
+        nthreads = (int)BH;
+    head_job *jobs = (head_job *)calloc((size_t)nthreads, sizeof(head_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    unsigned char *spawned = (unsigned char *)calloc((size_t)nthreads, 1);
+    if (!jobs || !tids || !spawned) {
+        free(jobs);
+        free(tids);
+        free(spawned);
+        return ORACLE_ENOMEM;
+    }
+    long per = (BH + nthreads - 1) / nthreads;
+    int status = ORACLE_OK;
+    for (int t = 0; t < nthreads; ++t) {
+        head_job *hj = &jobs[t];
+        hj->q = q; hj->k = k; hj->v = v; hj->g = g; hj->n = N; hj->d = d;
+        hj->scale = scale; hj->causal = causal; hj->dq = dq; hj->dk = dk; hj->dv = dv;
+        hj->begin = t * per;
+        hj->end = (t + 1) * per < BH ? (t + 1) * per : BH;
+        hj->status = ORACLE_OK;
+        if (hj->begin >= hj->end)
+            continue;
+        if (t < nthreads - 1 && pthread_create(&tids[t], NULL, head_worker, hj) == 0)
+            spawned[t] = 1;
+        else
+            head_worker(hj);
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (spawned[t])
+            pthread_join(tids[t], NULL);
+        if (jobs[t].status != ORACLE_OK)
+            status = jobs[t].status;
+    }
+    free(spawned);
+    free(jobs);
+    free(tids);
+    return status;
 }
 
 int oracle_abi_version(void) { return 1; }

@@ -11,7 +11,7 @@ Sources (page title, section):
     3.6.4  stable softmax, online recurrence, alpha <= 1, block-order independence
     3.6.5  worked example (tests/golden/p4_worked_example.json)
     3.6.6  causal: keys j > i are skipped
-    3.6.7  saved statistic L = m + log l
+    3.6.7  saved statistic L = m + log l; the backward pass recomputes S, P
     3.6.10 pitfalls: rescale both l and O; never drop the max shift
     3.6.11 exercise 2 (tests/golden/p4_exercise2.json)
 """
@@ -320,6 +320,114 @@ def pin_rows_agree_with_full(orc):
         _close(lse2, lse.reshape(B * H, N)[rows[:, 0], rows[:, 1]], 0.0, "rows vs full lse")
 
 
+# ---------------------------------------------------------------------------
+# Backward pass (section 3.6.7: gradients of the same definition).
+
+def _loss(orc, q, k, v, g, scale, causal):
+    o, _ = orc.attention_fwd(q, k, v, scale, causal=causal, threads=1)
+    return float(np.sum(o * g))
+
+
+def pin_bwd_finite_differences(orc):
+    """Every gradient entry matches a central difference of sum(o * g)
+    computed with the (separately pinned) forward oracle."""
+    rng = np.random.default_rng(4040)
+    B, H, N, d = 1, 2, 5, 3
+    q, k, v, g = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    h = 1e-5
+    for causal in (False, True):
+        grads = orc.attention_bwd(q, k, v, g, 0.7, causal=causal, threads=2)
+        for name, x, gx in zip("qkv", (q, k, v), grads):
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                up = _loss(orc, q, k, v, g, 0.7, causal)
+                x[idx] = old - h
+                dn = _loss(orc, q, k, v, g, 0.7, causal)
+                x[idx] = old
+                fd[idx] = (up - dn) / (2 * h)
+            _close(gx, fd, 1e-7, "d%s vs central difference (causal=%d)" % (name, causal))
+
+
+def pin_bwd_single_key(orc):
+    """N = 1: p = 1 whatever the score, so dv = g and dq = dk = 0."""
+    rng = np.random.default_rng(4141)
+    q, k, v, g = (rng.standard_normal((2, 1, 1, 4)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_bwd(q, k, v, g, 1.3, causal=causal)
+        _close(dv, g, 1e-15, "dv with one key")
+        _close(dq, np.zeros_like(q), 0.0, "dq with one key")
+        _close(dk, np.zeros_like(k), 0.0, "dk with one key")
+
+
+def pin_bwd_two_keys_closed_form(orc):
+    """N = 2, d = 1, non-causal: o_i = sig(a_i) v_0 + (1 - sig(a_i)) v_1 with
+    a_i = scale q_i (k_0 - k_1), so
+    do_i/dq_i = sig'(a_i) scale (k_0 - k_1)(v_0 - v_1)."""
+    q = np.array([0.8, -1.1]).reshape(1, 1, 2, 1)
+    k = np.array([0.4, -0.9]).reshape(1, 1, 2, 1)
+    v = np.array([2.0, -0.5]).reshape(1, 1, 2, 1)
+    g = np.array([1.5, 0.25]).reshape(1, 1, 2, 1)
+    scale = 0.6
+    dq, dk, dv = orc.attention_bwd(q, k, v, g, scale)
+    want_dq = np.zeros(2)
+    want_dv = np.zeros(2)
+    want_dk = np.zeros(2)
+    for i in range(2):
+        a = scale * q[0, 0, i, 0] * (k[0, 0, 0, 0] - k[0, 0, 1, 0])
+        sig = 1.0 / (1.0 + math.exp(-a))
+        ds = g[0, 0, i, 0] * sig * (1 - sig) * (v[0, 0, 0, 0] - v[0, 0, 1, 0])
+        want_dq[i] = ds * scale * (k[0, 0, 0, 0] - k[0, 0, 1, 0])
+        want_dk[0] += ds * scale * q[0, 0, i, 0]
+        want_dk[1] -= ds * scale * q[0, 0, i, 0]
+        want_dv[0] += sig * g[0, 0, i, 0]
+        want_dv[1] += (1 - sig) * g[0, 0, i, 0]
+    _close(dq.ravel(), want_dq, 1e-14, "two-key dq")
+    _close(dk.ravel(), want_dk, 1e-14, "two-key dk")
+    _close(dv.ravel(), want_dv, 1e-14, "two-key dv")
+
+
+def pin_bwd_sum_rules(orc):
+    """Rows of P sum to 1 and rows of dS sum to 0, so per head
+    sum_j dv_j = sum_i g_i and sum_j dk_j = 0; and since q and k enter only
+    through s_ij = scale <q_i, k_j>, sum <dq_i, q_i> = sum <dk_j, k_j>."""
+    rng = np.random.default_rng(4242)
+    B, H, N, d = 2, 2, 17, 6
+    q, k, v, g = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_bwd(q, k, v, g, 0.45, causal=causal, threads=3)
+        _close(dv.sum(axis=2), g.sum(axis=2), 1e-12, "sum of dv")
+        _close(dk.sum(axis=2), np.zeros((B, H, d)), 1e-12, "sum of dk")
+        _close(np.einsum("bhnd,bhnd->bh", dq, q), np.einsum("bhnd,bhnd->bh", dk, k), 1e-12,
+               "<dq,q> vs <dk,k>")
+
+
+def pin_bwd_value_shift(orc):
+    """Adding one vector c to every value row shifts every o_i by c, which
+    does not depend on q or k: dq and dk are unchanged, and so is dv."""
+    rng = np.random.default_rng(4343)
+    q, k, v, g = (rng.standard_normal((1, 2, 9, 4)) for _ in range(4))
+    c = rng.standard_normal(4) * 3.0
+    for causal in (False, True):
+        a = orc.attention_bwd(q, k, v, g, 0.5, causal=causal)
+        b = orc.attention_bwd(q, k, v + c, g, 0.5, causal=causal)
+        for name, x, y in zip(("dq", "dk", "dv"), a, b):
+            _close(x, y, 1e-12, "%s under a value shift" % name)
+
+
+def pin_bwd_causal_first_row(orc):
+    """Causal: row 0 sees only key 0, so dq_0 = 0, and the last key is seen
+    only by the last row, which makes dv_{N-1} = p_{N-1,N-1} g_{N-1}."""
+    rng = np.random.default_rng(4444)
+    q, k, v, g = (rng.standard_normal((1, 1, 6, 3)) for _ in range(4))
+    dq, _, dv = orc.attention_bwd(q, k, v, g, 0.9, causal=True)
+    _close(dq[0, 0, 0], np.zeros(3), 0.0, "causal dq_0")
+    s = 0.9 * q[0, 0, 5] @ k[0, 0].T
+    p_last = math.exp(s[5] - s.max()) / np.exp(s - s.max()).sum()
+    _close(dv[0, 0, 5], p_last * g[0, 0, 5], 1e-14, "causal dv of the last key")
+
+
 PINS = [
     pin_worked_example_full,
     pin_worked_example_online,
@@ -334,4 +442,10 @@ PINS = [
     pin_constant_values,
     pin_online_matches_two_pass,
     pin_rows_agree_with_full,
+    pin_bwd_finite_differences,
+    pin_bwd_single_key,
+    pin_bwd_two_keys_closed_form,
+    pin_bwd_sum_rules,
+    pin_bwd_value_shift,
+    pin_bwd_causal_first_row,
 ]

@@ -36,6 +36,19 @@ MUTATIONS = [
     ("online_no_max_shift", "pv += exp(s[j] - m_new) * v[j * d + c];", "pv += exp(s[j]) * v[j * d + c];"),
     ("online_no_final_normalise", "o_out[c] = acc[c] / l;", "o_out[c] = acc[c];"),
     ("row_slice_off_by_one", "jb->begin = t * per;", "jb->begin = t * per + (t > 0);"),
+    ("bwd_head_slice_off_by_one", "hj->begin = t * per;", "hj->begin = t * per + (t > 0);"),
+    ("bwd_dv_uses_ds", "dv[j * d + c] += s[j] * g[i * d + c];", "dv[j * d + c] += ds * g[i * d + c];"),
+    ("bwd_ds_not_centred", "double ds = s[j] * (dp[j] - pdp);", "double ds = s[j] * dp[j];"),
+    ("bwd_ds_sign", "double ds = s[j] * (dp[j] - pdp);", "double ds = s[j] * (pdp - dp[j]);"),
+    ("bwd_dq_no_scale", "dq[i * d + c] += scale * ds * k[j * d + c];",
+     "dq[i * d + c] += ds * k[j * d + c];"),
+    ("bwd_dk_uses_k", "dk[j * d + c] += scale * ds * q[i * d + c];",
+     "dk[j * d + c] += scale * ds * k[j * d + c];"),
+    ("bwd_dp_transposed", "dot += g[i * d + c] * v[j * d + c];", "dot += g[j * d + c] * v[i * d + c];"),
+    ("bwd_p_not_normalised", "s[j] = exp(s[j] - m) / row_sum;", "s[j] = exp(s[j] - m);"),
+    ("bwd_no_max_shift", "row_sum += exp(s[j] - m);", "row_sum += exp(s[j]);"),
+    ("bwd_head_offset_dropped", "job->n, job->d, job->scale, job->causal, s, dp, job->dq + bh * he,",
+     "job->n, job->d, job->scale, job->causal, s, dp, job->dq,"),
 ]
 
 
