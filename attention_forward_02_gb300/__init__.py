@@ -1,17 +1,19 @@
-"""GB300-native (sm_103a) FlashAttention-2 style attention forward.
+"""GB300-native (sm_103a) FlashAttention-2 style attention.
 
 ``fa_fwd(q, k, v, ...)`` computes O = softmax(Q K^T * scale) V and the row
 log-sum-exp for contiguous [B, H, N, d] fp16/bf16 CUDA tensors by calling the
-C ABI (include/fa.h) of the in-tree CUDA library on the current torch stream.
+C ABI (include/fa.h) of the in-tree CUDA library on the current torch stream;
+``fa_bwd`` computes the gradients of q, k, v from the forward's o and lse.
 PyTorch only supplies device memory and the stream; every step of the
 computation runs in the library's kernel.  There is no CPU or eager fallback:
 without the built library, or off a CUDA device, calls raise ``FAError``.
 """
 from ._lib import (FA_BF16, FA_FP16, FAError, fa1_fwd_raw, fa1_fwd_workspace_size,
-                   fa_abi_version, fa_fwd_raw, fa_last_device_status, fa_selftest_wait_timeout,
-                   fa_status_str, lib_path, load)
+                   fa_abi_version, fa_bwd_raw, fa_bwd_workspace_size, fa_fwd_raw,
+                   fa_last_device_status, fa_selftest_wait_timeout, fa_status_str, lib_path, load)
 
 __all__ = ["fa_fwd", "fa_fwd_raw", "fa1_fwd", "fa1_fwd_raw", "fa1_fwd_workspace_size",
+           "fa_bwd", "fa_bwd_raw", "fa_bwd_workspace_size",
            "fa_last_device_status", "fa_selftest_wait_timeout",
            "fa_status_str", "fa_abi_version", "FAError", "load", "lib_path"]
 
@@ -117,3 +119,48 @@ def fa_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, return_lse=True,
     if st != 0:
         raise FAError(st, "fa_fwd")
     return o, lse
+
+
+def fa_bwd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv=None,
+           workspace=None, stream=None):
+    """Attention backward: gradients (dq, dk, dv) of a loss given dout = dL/do.
+
+    q, k, v, o, dout: contiguous [B, H, N, d] CUDA tensors of one dtype (o the
+    forward output for q, k, v); lse: the forward's [B, H, N] fp32 log-sum-exp.
+    scale and causal must be the forward's.  dq/dk/dv: optional preallocated
+    outputs; workspace: optional CUDA uint8 tensor of at least
+    fa_bwd_workspace_size bytes (allocated with torch when None)."""
+    import torch
+    _check_qkv(q, k, v)
+    for name, t in (("o", o), ("dout", dout)):
+        if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.shape != q.shape
+                or t.dtype != q.dtype or not t.is_contiguous()):
+            raise FAError(1, "%s must be a contiguous CUDA tensor shaped and typed like q" % name)
+    B, H, N, d = q.shape
+    if (not isinstance(lse, torch.Tensor) or not lse.is_cuda or lse.shape != (B, H, N)
+            or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise FAError(1, "lse must be a contiguous CUDA float32 tensor of shape [B, H, N]")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = float(d) ** -0.5
+    outs = []
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t is None:
+            t = torch.empty_like(q)
+        elif t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous() or not t.is_cuda:
+            raise FAError(1, "%s must be a contiguous CUDA tensor shaped and typed like q" % name)
+        outs.append(t)
+    dq, dk, dv = outs
+    need = fa_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, N,
+                        d, float(scale), int(bool(causal)), code, stream.cuda_stream)
+    if st != 0:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv

@@ -19,8 +19,9 @@ FA_FP16 = 0
 FA_BF16 = 1
 
 # every symbol include/fa.h declares
-EXPORTS = ("fa_fwd", "fa1_fwd_workspace_size", "fa1_fwd", "fa1_fwd_noalloc", "fa_last_device_status",
-           "fa_selftest_wait_timeout", "fa_status_str", "fa_abi_version")
+EXPORTS = ("fa_fwd", "fa1_fwd_workspace_size", "fa1_fwd", "fa1_fwd_noalloc", "fa_bwd_workspace_size",
+           "fa_bwd", "fa_last_device_status", "fa_selftest_wait_timeout", "fa_status_str",
+           "fa_abi_version")
 
 _lib = None
 
@@ -57,6 +58,11 @@ def load(path=None):
     lib.fa1_fwd.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i, i, vp]
     lib.fa1_fwd_noalloc.restype = i
     lib.fa1_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i,
+                           i, vp]
     lib.fa_last_device_status.restype = i
     lib.fa_last_device_status.argtypes = [vp]
     lib.fa_selftest_wait_timeout.restype = i
@@ -85,6 +91,17 @@ def fa1_fwd_workspace_size(B, H, N, d):
 def fa1_fwd_raw(q, k, v, o, lse, ws, ws_bytes, B, H, N, d, scale, causal, dtype, stream):
     """Direct call of the FA1-structured entry point; returns the status."""
     return load().fa1_fwd(q, k, v, o, lse, ws, ws_bytes, B, H, N, d, scale, causal, dtype, stream)
+
+
+def fa_bwd_workspace_size(B, H, N, d):
+    return load().fa_bwd_workspace_size(B, H, N, d)
+
+
+def fa_bwd_raw(q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes, B, H, N, d, scale, causal, dtype,
+               stream):
+    """Direct call of the backward entry point; returns the status."""
+    return load().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes, B, H, N, d, scale, causal,
+                         dtype, stream)
 
 
 def fa_last_device_status(stream=None):

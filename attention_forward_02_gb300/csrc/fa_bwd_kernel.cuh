@@ -1,0 +1,609 @@
+// fa_bwd_kernel.cuh -- the sm_103a attention-backward kernels.
+//
+// What they compute: for one head with S = scale Q K^T (causal: key j > query
+// i masked), P = softmax(S) row by row, O = P V, and an upstream gradient dO,
+//   dV = P^T dO
+//   dP = dO V^T
+//   dS = P o (dP - D),  D_i = sum_c dO_ic O_ic  (= sum_j P_ij dP_ij)
+//   dQ = scale dS K,   dK = scale dS^T Q.
+// "3.6 어텐션 I — 메모리 문제·FlashAttention 원리", section 3.6.7: the backward
+// pass does not read a stored S or P; it recomputes them block by block from
+// Q, K and the row statistic L = m + log l that the forward pass saved
+// (P_ij = exp(S_ij - L_i)).
+//
+// Three launches:
+//   fa_bwd_prep_kernel  D_i and L_i * log2(e) into a padded per-head layout,
+//                       and zeroes the fp32 dQ accumulator.
+//   fa_bwd_kernel       one CTA per (batch*head, 128-key block): K_n and V_n
+//                       stay in shared memory; the CTA walks the query blocks
+//                       m (all of them, or m >= n when causal) and keeps dK_n
+//                       and dV_n in TMEM for the whole walk.  Per query block:
+//                         S^T  = K_n Q_m^T           (tcgen05, TMEM)
+//                         dP^T = V_n dO_m^T          (tcgen05, TMEM)
+//                         P^T  = 2^(S^T scale log2e - L_m log2e)   (warps 0-7)
+//                         dS^T = P^T o (dP^T - D_m) scale          (warps 0-7)
+//                         dV_n += P^T dO_m           (P^T read from TMEM)
+//                         dK_n += dS^T Q_m           (dS^T from shared memory)
+//                         dQ_m  = dS K_n             (the same shared tile, read
+//                                                     as an MN-major operand)
+//                       and warps 8-11 add dQ_m into the fp32 accumulator with
+//                       TMA reduce-add (other key blocks add to the same rows).
+//   fa_bwd_dq_kernel    rounds the fp32 accumulator to dQ in the input dtype.
+//
+// Warp roles in fa_bwd_kernel (512 threads):
+//   warps 0-3, 4-7  compute warpgroups c = 0, 1: thread r owns key row r (TMEM
+//                   lane r) for query columns [64c, 64c + 64) of the block.
+//   warps 8-11      dQ warpgroup: thread r owns query row r of dQ_m.
+//   warp 12         TMA producer; warp 13 MMA issuer (one thread).
+// Every mbarrier wait is bounded, as in the forward kernel.
+#pragma once
+
+#include "fa_common.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kBlk = 128;  // keys per CTA, queries per step
+constexpr int kThreads = 512;
+constexpr int kDqWarp0 = 8;
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: S^T @ 0 (P^T, 16-bit, over its first columns), dP^T @ 128,
+// dV @ 256, dK @ 256 + D, dQ @ 384 for D = 64; for D = 128 dQ_m takes the dP^T
+// columns, which the compute warps have finished reading when dQ_m is issued.
+constexpr uint32_t kTmS = 0;
+constexpr uint32_t kTmDP = 128;
+constexpr uint32_t kTmDV = 256;
+template <int D>
+__host__ __device__ constexpr uint32_t col_dk()
+{
+    return 256u + D;
+}
+template <int D>
+__host__ __device__ constexpr uint32_t col_dq()
+{
+    return D == 64 ? 384u : kTmDP;
+}
+// TMEM column of K step t (queries 16t .. 16t + 15) of P^T: compute
+// warpgroup c writes the P^T of its queries [64c, 64c + 64) over S^T columns
+// [64c, 64c + 32), which it has already read.
+__host__ __device__ constexpr uint32_t tm_p_step(int t)
+{
+    return kTmS + 64u * (t >> 2) + 8u * (t & 3);
+}
+
+template <int D>
+struct Cfg {
+    static constexpr int TILE = kBlk * D * 2;  // one [128, D] 16-bit tile
+    static constexpr int QST = 2;              // Q (+ L) ring
+    static constexpr int DOST = D == 64 ? 2 : 1;  // dO (+ D) ring
+    static constexpr int NSTG = D == 64 ? 2 : 1;  // dQ staging buffers
+    static constexpr int STG_BYTES = kBlk * 32 * 4;  // [128 rows x 32 fp32], 128B-swizzled
+    static constexpr bool DQ_ALIAS = D == 128;
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = K_OFF + TILE;
+    static constexpr int Q_OFF = V_OFF + TILE;
+    static constexpr int DO_OFF = Q_OFF + QST * TILE;
+    static constexpr int DS_OFF = DO_OFF + DOST * TILE;  // dS^T [128 keys x 128 queries]
+    static constexpr int STG_OFF = DS_OFF + kBlk * kBlk * 2;
+    static constexpr int L_OFF = STG_OFF + NSTG * STG_BYTES;  // QST x 128 fp32
+    static constexpr int DD_OFF = L_OFF + QST * kBlk * 4;      // DOST x 128 fp32
+    static constexpr int BAR_OFF = DD_OFF + DOST * kBlk * 4;
+    static constexpr int B_KVFULL = 0;
+    static constexpr int B_QFULL = 1;
+    static constexpr int B_QEMPTY = B_QFULL + QST;
+    static constexpr int B_DOFULL = B_QEMPTY + QST;
+    static constexpr int B_DOEMPTY = B_DOFULL + DOST;
+    static constexpr int B_SFULL = B_DOEMPTY + DOST;
+    static constexpr int B_DPFULL = B_SFULL + 1;
+    static constexpr int B_PFULL = B_DPFULL + 1;
+    static constexpr int B_DSFULL = B_PFULL + 1;
+    static constexpr int B_DQFULL = B_DSFULL + 1;
+    static constexpr int B_DQFREE = B_DQFULL + 1;
+    static constexpr int B_DKVFULL = B_DQFREE + 1;
+    static constexpr int B_DRAIN = B_DKVFULL + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // TMEM base address, abort flag
+    static constexpr int SMEM_USED = SLOT_OFF + 16;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+    static_assert(DS_OFF % 1024 == 0 && STG_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+};
+
+// Work item of CTA w: (head bh, key block n).  Causal: the heaviest key blocks
+// (low n, which see the most query blocks) of every head first.  Non-causal:
+// head-major, so CTAs running together share one head's Q and dO in L2.
+template <bool CAUSAL>
+__device__ __forceinline__ void item_coords(int w, int BH, int nb, int &bh, int &n)
+{
+    if (CAUSAL) {
+        n = w / BH;
+        bh = w % BH;
+    } else {
+        bh = w / nb;
+        n = w % nb;
+    }
+}
+
+template <int D, bool CAUSAL, typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                  const __grid_constant__ CUtensorMap tm_dqacc, const float *__restrict__ lse2,
+                  const float *__restrict__ dvec, int N, int Npad, int BH, int nb, float scale,
+                  float scale_log2)
+{
+    using C = Cfg<D>;
+    constexpr int QST = C::QST;
+    constexpr int DOST = C::DOST;
+    constexpr int NSTG = C::NSTG;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int bh, n;
+    item_coords<CAUSAL>(static_cast<int>(blockIdx.x), BH, nb, bh, n);
+    const int m0 = CAUSAL ? n : 0;  // first query block that sees key block n
+    const int cnt = nb - m0;        // query blocks walked (>= 1)
+
+    auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + C::SLOT_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SLOT_OFF + 4);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_KVFULL), 1);
+        for (int s = 0; s < QST; ++s) {
+            mbar_init(bar(C::B_QFULL + s), 1);
+            mbar_init(bar(C::B_QEMPTY + s), 1);
+        }
+        for (int s = 0; s < DOST; ++s) {
+            mbar_init(bar(C::B_DOFULL + s), 1);
+            mbar_init(bar(C::B_DOEMPTY + s), 1);
+        }
+        mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_DPFULL), 1);
+        mbar_init(bar(C::B_PFULL), 2 * 128);
+        mbar_init(bar(C::B_DSFULL), 2 * 128);
+        mbar_init(bar(C::B_DQFULL), 1);
+        mbar_init(bar(C::B_DQFREE), 128);
+        mbar_init(bar(C::B_DKVFULL), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            // ---------------- producer ----------------
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+            // K_n, V_n are read by this CTA only; Q_m, dO_m by every key block
+            // of the head.
+            const uint64_t pol_kv = l2_policy_evict_first();
+            const uint64_t pol_q = l2_policy_evict_last();
+            mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
+            for (int b = 0; b < D / 64; ++b) {
+                tma_load_3d(sbase + C::K_OFF + b * kSwAtomBytes, &tm_k, bar(C::B_KVFULL), b * 64, n * kBlk,
+                            bh, pol_kv);
+                tma_load_3d(sbase + C::V_OFF + b * kSwAtomBytes, &tm_v, bar(C::B_KVFULL), b * 64, n * kBlk,
+                            bh, pol_kv);
+            }
+            int nq = 0, ndo = 0;
+            bool ok = true;
+            for (int i = 0; ok && i < cnt; ++i) {
+                const int m = m0 + i;
+                const size_t row0 = static_cast<size_t>(bh) * Npad + static_cast<size_t>(m) * kBlk;
+                const int s = i % QST;
+                if (i >= QST && !(ok = wait_bounded(bar(C::B_QEMPTY + s), ((i / QST) - 1) & 1, abort_flag)))
+                    break;
+                mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE + kBlk * 4);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(sbase + C::Q_OFF + s * C::TILE + b * kSwAtomBytes, &tm_q, bar(C::B_QFULL + s),
+                                b * 64, m * kBlk, bh, pol_q);
+                bulk_load(sbase + C::L_OFF + s * kBlk * 4, lse2 + row0, kBlk * 4, bar(C::B_QFULL + s));
+                ++nq;
+                const int ds = i % DOST;
+                if (i >= DOST && !(ok = wait_bounded(bar(C::B_DOEMPTY + ds), ((i / DOST) - 1) & 1, abort_flag)))
+                    break;
+                mbar_arrive_expect_tx(bar(C::B_DOFULL + ds), C::TILE + kBlk * 4);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(sbase + C::DO_OFF + ds * C::TILE + b * kSwAtomBytes, &tm_do,
+                                bar(C::B_DOFULL + ds), b * 64, m * kBlk, bh, pol_q);
+                bulk_load(sbase + C::DD_OFF + ds * kBlk * 4, dvec + row0, kBlk * 4, bar(C::B_DOFULL + ds));
+                ++ndo;
+            }
+            // wait for every copy this thread issued
+            drain_bounded(bar(C::B_KVFULL), 0);
+            for (int s = 0; s < QST; ++s)
+                if (nq > s)
+                    drain_bounded(bar(C::B_QFULL + s), ((nq - 1 - s) / QST) & 1);
+            for (int s = 0; s < DOST; ++s)
+                if (ndo > s)
+                    drain_bounded(bar(C::B_DOFULL + s), ((ndo - 1 - s) / DOST) & 1);
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr bool BF = DTypeTraits<T>::kBF16;
+            constexpr uint32_t idesc_s = make_idesc_f16(BF, kBlk, kBlk, false, false);
+            constexpr uint32_t idesc_acc = make_idesc_f16(BF, kBlk, D, false, true);
+            constexpr uint32_t idesc_dq = make_idesc_f16(BF, kBlk, D, true, true);
+            // K-major views (operands whose contraction runs along the row) and
+            // MN-major views (contraction down the rows) of the same tiles.
+            const uint64_t k_kmaj = make_sdesc_sw128(sbase + C::K_OFF, 16, 1024);
+            const uint64_t k_mn = make_sdesc_sw128(sbase + C::K_OFF, kSwAtomBytes, 1024);
+            const uint64_t v_kmaj = make_sdesc_sw128(sbase + C::V_OFF, 16, 1024);
+            const uint64_t q_kmaj = make_sdesc_sw128(sbase + C::Q_OFF, 16, 1024);
+            const uint64_t q_mn = make_sdesc_sw128(sbase + C::Q_OFF, kSwAtomBytes, 1024);
+            const uint64_t do_kmaj = make_sdesc_sw128(sbase + C::DO_OFF, 16, 1024);
+            const uint64_t do_mn = make_sdesc_sw128(sbase + C::DO_OFF, kSwAtomBytes, 1024);
+            const uint64_t ds_kmaj = make_sdesc_sw128(sbase + C::DS_OFF, 16, 1024);
+            const uint64_t ds_mn = make_sdesc_sw128(sbase + C::DS_OFF, kSwAtomBytes, 1024);
+            // K step kk: 16 elements along the row (K-major: 32 bytes inside a
+            // 64-column swizzle block, then the next block), or 16 rows
+            // (MN-major: 2048 bytes).
+            auto kmaj = [](int kk) -> uint32_t {
+                return static_cast<uint32_t>(((kk >> 2) * kSwAtomBytes + (kk & 3) * 32) >> 4);
+            };
+            auto mn = [](int kk) -> uint32_t { return static_cast<uint32_t>((kk * 2048) >> 4); };
+            auto tile = [](int slot) -> uint32_t { return static_cast<uint32_t>((slot * C::TILE) >> 4); };
+
+            auto issue_s = [&](int s) {  // S^T = K Q^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_f16_ss(tmem + kTmS, k_kmaj + kmaj(kk), q_kmaj + tile(s) + kmaj(kk), idesc_s,
+                                kk > 0 ? 1u : 0u);
+            };
+            auto issue_dp = [&](int s) {  // dP^T = V dO^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_f16_ss(tmem + kTmDP, v_kmaj + kmaj(kk), do_kmaj + tile(s) + kmaj(kk), idesc_s,
+                                kk > 0 ? 1u : 0u);
+            };
+            auto issue_dv = [&](int s, bool acc) {  // dV += P^T dO
+#pragma unroll
+                for (int kk = 0; kk < kBlk / 16; ++kk)
+                    umma_f16_ts(tmem + kTmDV, tmem + tm_p_step(kk), do_mn + tile(s) + mn(kk), idesc_acc,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            auto issue_dk = [&](int s, bool acc) {  // dK += dS^T Q
+#pragma unroll
+                for (int kk = 0; kk < kBlk / 16; ++kk)
+                    umma_f16_ss(tmem + col_dk<D>(), ds_kmaj + kmaj(kk), q_mn + tile(s) + mn(kk), idesc_acc,
+                                (acc || kk > 0) ? 1u : 0u);
+            };
+            auto issue_dq = [&]() {  // dQ = dS K
+#pragma unroll
+                for (int kk = 0; kk < kBlk / 16; ++kk)
+                    umma_f16_ss(tmem + col_dq<D>(), ds_mn + mn(kk), k_mn + mn(kk), idesc_dq, kk > 0 ? 1u : 0u);
+            };
+
+            bool ok = wait_bounded(bar(C::B_KVFULL), 0, abort_flag) &&
+                      wait_bounded(bar(C::B_QFULL), 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                umma_commit(bar(C::B_SFULL));
+                ok = wait_bounded(bar(C::B_DOFULL), 0, abort_flag);
+            }
+            if (ok) {
+                tc_fence_after();
+                issue_dp(0);
+                umma_commit(bar(C::B_DPFULL));
+            }
+            for (int i = 0; ok && i < cnt; ++i) {
+                const int s = i % QST, ds = i % DOST;
+                const uint32_t ph = static_cast<uint32_t>(i & 1);
+                if (!(ok = wait_bounded(bar(C::B_PFULL), ph, abort_flag)))
+                    break;
+                tc_fence_after();
+                issue_dv(ds, i > 0);
+                if (i + 1 < cnt) {
+                    // S^T of the next block overwrites P^T, after the dV product
+                    // above has read it (one thread's MMAs run in issue order)
+                    const int s1 = (i + 1) % QST;
+                    if (!(ok = wait_bounded(bar(C::B_QFULL + s1), ((i + 1) / QST) & 1, abort_flag)))
+                        break;
+                    tc_fence_after();
+                    issue_s(s1);
+                    umma_commit(bar(C::B_SFULL));
+                }
+                if (!(ok = wait_bounded(bar(C::B_DSFULL), ph, abort_flag)))
+                    break;
+                tc_fence_after();
+                // the compute warps are done with D_m; dP^T and dV have read dO_m
+                umma_commit(bar(C::B_DOEMPTY + ds));
+                issue_dk(s, i > 0);
+                if (!C::DQ_ALIAS && i > 0) {
+                    if (!(ok = wait_bounded(bar(C::B_DQFREE), (i - 1) & 1, abort_flag)))
+                        break;
+                    tc_fence_after();
+                }
+                issue_dq();
+                umma_commit(bar(C::B_DQFULL));
+                umma_commit(bar(C::B_QEMPTY + s));
+                if (i + 1 < cnt) {
+                    if (C::DQ_ALIAS) {
+                        // dQ_m sits in the dP^T columns: wait until it is read out
+                        if (!(ok = wait_bounded(bar(C::B_DQFREE), ph, abort_flag)))
+                            break;
+                    }
+                    const int ds1 = (i + 1) % DOST;
+                    if (!(ok = wait_bounded(bar(C::B_DOFULL + ds1), ((i + 1) / DOST) & 1, abort_flag)))
+                        break;
+                    tc_fence_after();
+                    issue_dp(ds1);
+                    umma_commit(bar(C::B_DPFULL));
+                }
+            }
+            if (ok)
+                umma_commit(bar(C::B_DKVFULL));
+            // every MMA this thread issued has completed once this arrives
+            umma_commit(bar(C::B_DRAIN));
+            drain_bounded(bar(C::B_DRAIN), 0);
+        }
+    } else if (warp >= kDqWarp0 && warp < kDqWarp0 + 4) {
+        // ---------------- dQ warpgroup ----------------
+        const int r = threadIdx.x & 127;  // query row of the block == TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t dq_tm = tmem + lane_base + col_dq<D>();
+        const bool leader = threadIdx.x == kDqWarp0 * 32;
+        int chunk = 0;
+        for (int i = 0; i < cnt; ++i) {
+            bool ok = wait_bounded(bar(C::B_DQFULL), static_cast<uint32_t>(i & 1), abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (named_bar_or(3, 128, !ok))
+                break;
+            tc_fence_after();
+            const int m = m0 + i;
+#pragma unroll 1
+            for (int c4 = 0; c4 < D / 32; ++c4, ++chunk) {
+                uint32_t u[32];
+                tmem_ld32(dq_tm + 32 * c4, u);
+                if (c4 == D / 32 - 1) {
+                    // dQ_m has been read out: its TMEM columns are free
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_DQFREE));
+                }
+                const int stg = chunk % NSTG;
+                const uint32_t sbuf = sbase + C::STG_OFF + stg * C::STG_BYTES;
+                // the reduce that last read this staging buffer has finished reading
+                if (leader && chunk >= NSTG)
+                    bulk_wait_group_read<NSTG - 1>();
+                named_bar_sync(3, 128);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_shared_v4(sbuf + r * 128 + (((k ^ (r & 7)) & 7) << 4), u[4 * k], u[4 * k + 1],
+                                 u[4 * k + 2], u[4 * k + 3]);
+                fence_proxy_async_smem();
+                named_bar_sync(3, 128);
+                if (leader) {
+                    tma_reduce_add_3d(&tm_dqacc, sbuf, 32 * c4, m * kBlk, bh);
+                    bulk_commit_group();
+                }
+            }
+        }
+        if (leader)
+            bulk_wait_group<0>();
+    } else if (warp < 8) {
+        // ---------------- compute warpgroup c ----------------
+        const int c = warp >> 2;
+        const int r = threadIdx.x & 127;  // key row of the block == TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_tm = tmem + lane_base + kTmS;
+        const uint32_t dp_tm = tmem + lane_base + kTmDP;
+        const bool row_valid = n * kBlk + r < N;
+        const uint32_t ds_row = sbase + C::DS_OFF + c * kSwAtomBytes + r * 128;
+        const float2 c2 = make_float2(scale_log2, scale_log2);
+        const float2 sc = make_float2(scale, scale);
+        bool ok = true;
+        for (int i = 0; i < cnt; ++i) {
+            const int m = m0 + i;
+            const int s = i % QST, ds = i % DOST;
+            const uint32_t ph = static_cast<uint32_t>(i & 1);
+            ok = wait_bounded(bar(C::B_SFULL), ph, abort_flag) &&
+                 wait_bounded(bar(C::B_QFULL + s), (i / QST) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            tc_fence_after();
+            // ---- P^T for queries [64c, 64c + 64) of this key row ----
+            const bool diag = CAUSAL && m == n;  // keys above the query are masked
+            const float *lrow = reinterpret_cast<const float *>(smem + C::L_OFF + s * kBlk * 4);
+            uint32_t pk[32];
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t u[32];
+                tmem_ld32(s_tm + 64 * c + 32 * ch, u);
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const int q = 64 * c + 32 * ch + j;
+                    const float2 l2 = *reinterpret_cast<const float2 *>(lrow + q);
+                    const float2 x = ffma2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])), c2,
+                                           make_float2(-l2.x, -l2.y));
+                    float e0 = ex2_approx(x.x);
+                    float e1 = ex2_approx(x.y);
+                    if (diag) {
+                        e0 = (q >= r) ? e0 : 0.f;
+                        e1 = (q + 1 >= r) ? e1 : 0.f;
+                    }
+                    pk[16 * ch + j / 2] = DTypeTraits<T>::pack(e0, e1);
+                }
+                if (!row_valid) {
+                    // key past the sequence end (K row read as zeros): no weight
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[16 * ch + j] = 0u;
+                }
+                tmem_st16(s_tm + 64 * c + 16 * ch, reinterpret_cast<const uint32_t(&)[16]>(pk[16 * ch]));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));
+
+            // ---- dS^T = P^T o (dP^T - D) scale, into shared memory ----
+            ok = wait_bounded(bar(C::B_DPFULL), ph, abort_flag) &&
+                 wait_bounded(bar(C::B_DOFULL + ds), (i / DOST) & 1, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const float *drow = reinterpret_cast<const float *>(smem + C::DD_OFF + ds * kBlk * 4);
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t u[32];
+                tmem_ld32(dp_tm + 64 * c + 32 * ch, u);
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const int q = 64 * c + 32 * ch + j;
+                    const float2 dd = *reinterpret_cast<const float2 *>(drow + q);
+                    const float2 p = DTypeTraits<T>::unpack(pk[16 * ch + j / 2]);
+                    const float2 t = fadd2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])),
+                                           make_float2(-dd.x, -dd.y));
+                    const float2 g = fmul2(fmul2(p, sc), t);
+                    w[j / 2] = DTypeTraits<T>::pack(g.x, g.y);
+                }
+                // 16-byte chunk 4 ch + k of this row (8 queries each)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    st_shared_v4(ds_row + ((((4 * ch + k) ^ (r & 7)) & 7) << 4), w[4 * k], w[4 * k + 1],
+                                 w[4 * k + 2], w[4 * k + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_DSFULL));
+        }
+
+        // ---------------- epilogue: warpgroup 0 writes dV_n, warpgroup 1 dK_n ----------------
+        if (ok) {
+            ok = wait_bounded(bar(C::B_DKVFULL), 0, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        // both staging areas are free once every product has completed: the
+        // dS^T tile (last read by dQ) and Q slot 0 (last read by dK)
+        const uint32_t stage = sbase + (c == 0 ? C::DS_OFF : C::Q_OFF);
+        const uint32_t acc_tm = tmem + lane_base + (c == 0 ? kTmDV : col_dk<D>());
+        const bool bad = named_bar_or(1 + c, 128, !ok || *abort_flag != 0);
+        if (!bad) {
+            tc_fence_after();
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                uint32_t u[32];
+                tmem_ld32(acc_tm + 32 * c4, u);
+                const float *f = reinterpret_cast<const float *>(u);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    st_shared_v4(stage + sw128_offset(r, c4 * 4 + q4),
+                                 DTypeTraits<T>::pack(f[8 * q4 + 0], f[8 * q4 + 1]),
+                                 DTypeTraits<T>::pack(f[8 * q4 + 2], f[8 * q4 + 3]),
+                                 DTypeTraits<T>::pack(f[8 * q4 + 4], f[8 * q4 + 5]),
+                                 DTypeTraits<T>::pack(f[8 * q4 + 6], f[8 * q4 + 7]));
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + c, 128);
+            if (r == 0) {
+                for (int b = 0; b < D / 64; ++b)
+                    tma_store_3d(c == 0 ? &tm_dv : &tm_dk, stage + b * kSwAtomBytes, b * 64, n * kBlk, bh);
+                bulk_commit_group();
+                bulk_wait_group<0>();
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// D_i = sum_c dO_ic O_ic and L_i log2(e) for every row of a padded
+// [BH, Npad] layout (padding rows: D = 0, L = +inf, so P = 0 there), and the
+// fp32 dQ accumulator [BH, Npad, D] set to zero.  D / 8 threads per row, 8
+// elements (16 bytes) each.
+template <int D, typename T>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const T *__restrict__ o, const T *__restrict__ dout,
+                                                          const float *__restrict__ lse,
+                                                          float *__restrict__ lse2, float *__restrict__ dvec,
+                                                          float *__restrict__ dqacc, int N, int Npad,
+                                                          long long rows)
+{
+    constexpr int TPR = D / 8;
+    const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long row = g / TPR;
+    const int part = static_cast<int>(g % TPR);
+    const bool valid = row < rows;
+    const long long bh = valid ? row / Npad : 0;
+    const int i = valid ? static_cast<int>(row % Npad) : 0;
+    const bool live = valid && i < N;
+    float acc = 0.f;
+    if (live) {
+        const size_t off = (static_cast<size_t>(bh) * N + i) * D + part * 8;
+        const uint4 a = *reinterpret_cast<const uint4 *>(o + off);
+        const uint4 b = *reinterpret_cast<const uint4 *>(dout + off);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 x = DTypeTraits<T>::unpack(aw[k]);
+            const float2 y = DTypeTraits<T>::unpack(bw[k]);
+            acc = fmaf(x.x, y.x, acc);
+            acc = fmaf(x.y, y.y, acc);
+        }
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (valid) {
+        if (part == 0) {
+            dvec[row] = live ? acc : 0.f;
+            lse2[row] = live ? lse[static_cast<size_t>(bh) * N + i] * 1.4426950408889634f : INFINITY;
+        }
+        float4 *z = reinterpret_cast<float4 *>(dqacc + static_cast<size_t>(row) * D + part * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// dQ [BH, N, D] in the input dtype from the fp32 accumulator [BH, Npad, D].
+template <int D, typename T>
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float *__restrict__ dqacc, T *__restrict__ dq,
+                                                        int N, int Npad, long long chunks)
+{
+    constexpr int CPR = D / 8;  // 8-element chunks per row
+    for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < chunks;
+         g += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = g / CPR;  // row of [BH * N]
+        const int part = static_cast<int>(g % CPR);
+        const long long bh = row / N;
+        const int i = static_cast<int>(row % N);
+        const float4 *src = reinterpret_cast<const float4 *>(
+            dqacc + (static_cast<size_t>(bh) * Npad + i) * D + part * 8);
+        const float4 a = src[0], b = src[1];
+        *reinterpret_cast<uint4 *>(dq + static_cast<size_t>(row) * D + part * 8) =
+            make_uint4(DTypeTraits<T>::pack(a.x, a.y), DTypeTraits<T>::pack(a.z, a.w),
+                       DTypeTraits<T>::pack(b.x, b.y), DTypeTraits<T>::pack(b.z, b.w));
+    }
+}
+
+}  // namespace bwd
+}  // namespace fa

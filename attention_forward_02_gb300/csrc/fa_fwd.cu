@@ -12,15 +12,13 @@
 #include "fa.h"
 #include "fa1_fwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
+#include "fa_host.h"
+
+using fa_host::EncodeTiledFn;
+using fa_host::kMaxDevices;
+using fa_host::overlaps;
 
 namespace {
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     std::once_flag once;
@@ -87,6 +85,40 @@ void init_device(int dev, DeviceState &st)
     st.init_status = (e == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
 }
 
+
+
+// Persistent launch: one CTA per SM (TMEM and shared memory allow one), each
+// walking its share of the (batch*head, 256-row Q block) work items.
+template <int D, bool CAUSAL, typename T>
+fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
+                   float *lse, int BH, int N, float scale, int num_sms, cudaStream_t stream)
+{
+    const int num_q_blocks = (N + fa::kBM - 1) / fa::kBM;
+    const long long items = static_cast<long long>(BH) * num_q_blocks;
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
+    fa::fa_fwd_kernel<D, CAUSAL, T><<<grid, fa::kNumThreads, fa::KCfg<D>::SMEM_ALLOC, stream>>>(
+        mq, mk, mv, static_cast<T *>(o), lse, N, BH, num_q_blocks, scale, scale_log2);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, bool CAUSAL, typename T>
+fa_status_t launch_fa1(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
+                       float *lse, float *ws, int BH, int N, float scale, cudaStream_t stream)
+{
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    fa::fa1::fa1_fwd_kernel<D, CAUSAL, T>
+        <<<static_cast<unsigned>(BH), fa::fa1::kThreads, fa::fa1::Cfg<D>::SMEM_ALLOC, stream>>>(
+            mq, mk, mv, static_cast<T *>(o), lse, ws, N, scale, scale_log2);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+
+
+}  // namespace
+
+namespace fa_host {
+
 fa_status_t device_state(DeviceState **out)
 {
     int dev = -1;
@@ -118,34 +150,6 @@ fa_status_t encode_qkv_map(EncodeTiledFn encode, CUtensorMap *map, const void *p
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
-
-// Persistent launch: one CTA per SM (TMEM and shared memory allow one), each
-// walking its share of the (batch*head, 256-row Q block) work items.
-template <int D, bool CAUSAL, typename T>
-fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
-                   float *lse, int BH, int N, float scale, int num_sms, cudaStream_t stream)
-{
-    const int num_q_blocks = (N + fa::kBM - 1) / fa::kBM;
-    const long long items = static_cast<long long>(BH) * num_q_blocks;
-    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
-    fa::fa_fwd_kernel<D, CAUSAL, T><<<grid, fa::kNumThreads, fa::KCfg<D>::SMEM_ALLOC, stream>>>(
-        mq, mk, mv, static_cast<T *>(o), lse, N, BH, num_q_blocks, scale, scale_log2);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-}
-
-template <int D, bool CAUSAL, typename T>
-fa_status_t launch_fa1(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
-                       float *lse, float *ws, int BH, int N, float scale, cudaStream_t stream)
-{
-    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    fa::fa1::fa1_fwd_kernel<D, CAUSAL, T>
-        <<<static_cast<unsigned>(BH), fa::fa1::kThreads, fa::fa1::Cfg<D>::SMEM_ALLOC, stream>>>(
-            mq, mk, mv, static_cast<T *>(o), lse, ws, N, scale, scale_log2);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-}
-
-bool overlaps(uintptr_t a, size_t na, uintptr_t b, size_t nb) { return a < b + nb && b < a + na; }
 
 // Checks shared by the entry points; nothing here calls CUDA.  Sets *empty for
 // a problem with nothing to compute.
@@ -198,6 +202,26 @@ fa_status_t check_args(const void *q, const void *k, const void *v, const void *
     }
     return FA_OK;
 }
+
+fa_status_t encoder(EncodeTiledFn *fn, int *num_sms)
+{
+    DeviceState *st = nullptr;
+    fa_status_t s = device_state(&st);
+    if (s != FA_OK)
+        return s;
+    *fn = st->encode;
+    if (num_sms)
+        *num_sms = st->num_sms;
+    return FA_OK;
+}
+
+}  // namespace fa_host
+
+namespace {
+
+using fa_host::check_args;
+using fa_host::device_state;
+using fa_host::encode_qkv_map;
 
 // Device state plus the three TMA descriptors of Q, K, V.
 fa_status_t prepare(const void *q, const void *k, const void *v, int BH, int N, int d,
@@ -366,6 +390,10 @@ fa_status_t fa_last_device_status(void *stream)
         return FA_ERR_CUDA;
     if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess)
         return FA_ERR_CUDA;
+    unsigned int bwd_word = 0;
+    if (fa_host::take_bwd_status(&bwd_word) != FA_OK)
+        return FA_ERR_CUDA;
+    word |= bwd_word;
     if (word & ~fa::kStatusTimeout)
         return FA_ERR_CUDA;  // a self-test wait did not behave as required
     return (word & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;

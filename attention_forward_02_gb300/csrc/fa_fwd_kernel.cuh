@@ -43,14 +43,9 @@
 
 #include <cstdint>
 
-#include "sm100_ptx.cuh"
+#include "fa_common.cuh"
 
 namespace fa {
-
-// Device status word (one per device that loads the library): bit 0 = a
-// bounded wait expired.
-__device__ unsigned int g_fa_status;
-constexpr unsigned int kStatusTimeout = 1u;
 
 constexpr int kSubM = 128;          // rows per sub-tile (one M = 128 MMA; one TMEM lane per row)
 constexpr int kBM = 2 * kSubM;      // query rows per CTA
@@ -79,8 +74,6 @@ __host__ __device__ constexpr uint32_t tmem_p_col(int h)
     return D == 64 ? 384u + 64u * h : 128u * h;
 }
 constexpr float kRescaleLog2 = 8.0f;
-constexpr long long kWaitLimitCycles = 1ll << 31;  // about one second at 2 GHz
-constexpr int kSwAtomBytes = 128 * 128;             // [128 rows x 64 cols] 16-bit swizzle block
 
 template <int D>
 struct KCfg {
@@ -113,71 +106,6 @@ struct KCfg {
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * D <= static_cast<int>(kTmemCols), "TMEM budget");
 };
-
-template <typename T>
-struct DTypeTraits;
-template <>
-struct DTypeTraits<__half> {
-    static constexpr bool kBF16 = false;
-    static __device__ __forceinline__ uint32_t pack(float a, float b)
-    {
-        __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-};
-template <>
-struct DTypeTraits<__nv_bfloat16> {
-    static constexpr bool kBF16 = true;
-    static __device__ __forceinline__ uint32_t pack(float a, float b)
-    {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-};
-
-// Bounded wait.  Returns false if the CTA is aborting or the limit expired
-// (then the abort flag and the device status word are set).
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             long long limit_cycles = kWaitLimitCycles)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (*abort_flag)
-            return false;
-        if (clock64() - t0 > limit_cycles) {
-            *abort_flag = 1;
-            atomicOr(&g_fa_status, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
-// Bounded wait used on the way out (ignores the abort flag: it waits for
-// work this thread itself started).
-__device__ __forceinline__ void drain_bounded(uint32_t bar, uint32_t parity)
-{
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitLimitCycles) {
-            atomicOr(&g_fa_status, kStatusTimeout);
-            return;
-        }
-    }
-}
-
-// Byte offset of 16-byte chunk `chunk` of row `row` in a [128, 64*k] 16-bit
-// tile stored as k column blocks of [128 rows x 128 B], each 128B-swizzled
-// (chunk index XOR row % 8): the layout TMA SWIZZLE_128B writes and the
-// tcgen05 SW128 descriptors read.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
-{
-    return static_cast<uint32_t>((chunk >> 3) * kSwAtomBytes + row * 128 +
-                                 (((chunk & 7) ^ (row & 7)) << 4));
-}
 
 // Masks keys c >= limit of one row of scores (set to -inf).
 __device__ __forceinline__ void mask_tail(float (&s)[kBN], int limit)

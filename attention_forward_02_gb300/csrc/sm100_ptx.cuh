@@ -2,7 +2,8 @@
 // built here for sm_103a) features the attention kernel uses: mbarriers,
 // TMA tensor loads, tcgen05 MMA / TMEM allocation / TMEM loads and stores,
 // and the proxy / tcgen05 ordering fences.  Written from the PTX ISA
-// descriptions of these instructions.
+// descriptions of these instructions.  Also the bulk copies (plain, tensor
+// store, tensor reduce-add) the backward kernel uses.
 #pragma once
 
 #include <cstdint>
@@ -69,6 +70,58 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
+}
+
+// Plain bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Tensor store shared -> global of one box (rows outside the tensor are not
+// written), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int x, int y, int z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// Tensor reduce-add shared -> global of one box: global += shared, element
+// by element, performed in L2 (atomic with respect to other reductions).
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, uint32_t src, int x, int y, int z)
+{
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// At most N of this thread's bulk groups still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// At most N of this thread's bulk groups not yet complete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // L2 eviction-priority policies for the cache hint above.
@@ -294,6 +347,16 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&f)[128])
         "tcgen05.wait::ld.sync.aligned;\n\t}"
         : FA_R32(r), FA_R32((r + 32)), FA_R32((r + 64)), FA_R32((r + 96))
         : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 

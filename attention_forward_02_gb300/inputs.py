@@ -10,6 +10,9 @@ Recipe: Q, K, V are iid N(0, 1) drawn in fp32 by ``torch.Generator`` (CPU,
 two, so the product is exact in fp16/bf16), which spreads the scaled scores to
 a standard deviation of about 8 so that the running max keeps moving.
 
+The backward pass's upstream gradient dO follows the same recipe with a
+seed of its own (``make_dout``).
+
 Shapes follow the pages' [B, H, N, d] notation (contiguous, row stride d):
 "Triton으로 FlashAttention 1·2 forward 구현하기", section "기준 shape", uses
 [4, 32, 2048, 64] in fp16, and section "batch 크기에 따른 변화" varies B.
@@ -53,6 +56,14 @@ def make_qkv(B, H, N, d, dtype="fp16", seeds=(0, 1, 2), q_scale=1.0):
             x = x * q_scale
         out.append(x.contiguous())
     return tuple(out)
+
+
+def make_dout(B, H, N, d, dtype="fp16", seed=3):
+    """Upstream gradient dL/dO for the backward pass: iid N(0, 1) in fp32,
+    rounded to the 16-bit dtype, [B, H, N, d] on the CPU."""
+    dt = torch_dtype(dtype) if isinstance(dtype, str) else dtype
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    return torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(dt).contiguous()
 
 
 def make_workload(name, q_scale=1.0):

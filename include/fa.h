@@ -1,7 +1,7 @@
 /*
- * fa.h -- C ABI of the GB300 (sm_103a) attention-forward library.
+ * fa.h -- C ABI of the GB300 (sm_103a) attention library.
  *
- * One operation: the FlashAttention-2 style tiled attention forward
+ * The main operation: the FlashAttention-2 style tiled attention forward
  *
  *     O = softmax(Q K^T * scale) V,     LSE = log(sum_j exp(scale * q_i . k_j))
  *
@@ -14,7 +14,8 @@
  *    recurrence, alpha = exp(m_old - m_new), one final division by l), 3.6.6
  *    (the FA2 tile loop: Q block outer / parallel, K/V blocks inner; causal
  *    skips key blocks j > i and masks the diagonal block), 3.6.7 (row
- *    statistic L = m + log l saved for the backward pass).
+ *    statistic L = m + log l saved for the backward pass; the backward
+ *    pass, fa_bwd, recomputes S and P from it).
  *  - "Triton으로 FlashAttention 1·2 forward 구현하기", section "병렬화 단위":
  *    grid = (cdiv(N, BLOCK_M), B * H), one program per Q block.
  *  - "FlashAttention-2를 CuTe로 밑바닥부터 구현하며 겪은 GPU 커널 지옥기",
@@ -34,7 +35,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 1
+#define FA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define FA_API __attribute__((visibility("default")))
@@ -143,6 +144,54 @@ FA_API fa_status_t fa1_fwd(const void *q, const void *k, const void *v, void *o,
 FA_API fa_status_t fa1_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
                                    float *lse, int B, int H, int N, int d, float scale, int causal,
                                    fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_bwd_workspace_size -- bytes of device workspace fa_bwd needs: with
+ * Npad = N rounded up to a multiple of 128, an fp32 dQ accumulator
+ * [B*H, Npad, d] followed by two fp32 row vectors [B*H, Npad] (L log2(e) and
+ * D, see fa_bwd).  0 for invalid sizes.
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa_bwd -- attention backward on the caller's stream (asynchronous): the
+ * gradients of a loss with respect to q, k, v given its gradient dout with
+ * respect to the forward output o.  With S = scale Q K^T (causal: keys j > i
+ * masked), P = softmax(S), O = P V:
+ *     dV = P^T dO,   dP = dO V^T,   dS = P o (dP - D),  D_i = sum_c dO_ic O_ic,
+ *     dQ = scale dS K,   dK = scale dS^T Q.
+ * Following "3.6 어텐션 I — 메모리 문제·FlashAttention 원리", section 3.6.7,
+ * S and P are never read from memory: each 128 x 128 block is recomputed
+ * from Q, K and the forward pass's saved row statistic (P = exp(S - lse)).
+ *
+ *  q, k, v : the forward inputs; device, contiguous [B, H, N, d] of `dtype`,
+ *            16-byte aligned.  Read only.
+ *  o       : the forward output fa_fwd wrote for them (same layout).  Read only.
+ *  lse     : the forward's lse output, [B, H, N] fp32, 4-byte aligned; must
+ *            not be NULL.  Read only.
+ *  dout    : dL/dO, contiguous [B, H, N, d] of `dtype`, 16-byte aligned.
+ *  dq, dk, dv : outputs, contiguous [B, H, N, d] of `dtype`, 16-byte aligned;
+ *            must not overlap each other, the inputs or the workspace.
+ *            Written: the gradients rounded to nearest from fp32.
+ *  workspace : device pointer, 16-byte aligned, at least
+ *            fa_bwd_workspace_size(B, H, N, d) bytes, not overlapping any
+ *            other buffer; owned by the caller; contents on entry do not
+ *            matter (the call clears what it accumulates into).  Calls that
+ *            share a workspace must not run concurrently.
+ *  B, H, N, d, scale, causal, dtype, stream : as for fa_fwd (the same
+ *            values the forward call used).
+ *
+ * Three kernels run in order on `stream`: the row terms D and L log2(e) plus
+ * clearing the accumulator; the main kernel (one CTA per head and 128-key
+ * block, dK and dV kept on chip, dQ added into the fp32 accumulator); the
+ * rounding of dQ.  Errors: as fa_fwd, plus FA_ERR_INVALID_ARG for a NULL lse
+ * or dout/dq/dk/dv, or a missing, short or overlapping workspace, and
+ * FA_ERR_MISALIGNED for a misaligned buffer.
+ */
+FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                          const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                          void *workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                          float scale, int causal, fa_dtype_t dtype, void *stream);
 
 /*
  * fa_last_device_status -- synchronise `stream`, read and clear the device

@@ -99,6 +99,41 @@ def test_fa1_argument_checks(lib, kwargs, status):
     assert call_fa1(**kwargs) == status
 
 
+def test_bwd_workspace_size(lib):
+    # fp32 dQ accumulator [BH, Npad, d] + two fp32 row vectors, Npad = N rounded up to 128
+    assert fa.fa_bwd_workspace_size(4, 32, 2048, 64) == 4 * 32 * 2048 * 66 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 128) == 128 * 130 * 4
+    assert fa.fa_bwd_workspace_size(2, 3, 200, 64) == 6 * 256 * 66 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
+    assert fa.fa_bwd_workspace_size(1, -1, 1, 64) == 0
+
+
+DO, DQ, DK, DV = 0x70000000, 0x80000000, 0x90000000, 0xA0000000
+
+
+def call_bwd(ws=W, ws_bytes=1 << 30, **kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, do=DO, dq=DQ, dk=DK, dv=DV, B=1, H=2, N=256, d=64,
+             scale=0.125, causal=0, dtype=0)
+    a.update(kw)
+    return fa.fa_bwd_raw(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
+                         a["dv"], ws, ws_bytes, a["B"], a["H"], a["N"], a["d"], a["scale"],
+                         a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(lse=0), 1), (dict(do=0), 1), (dict(dq=0), 1), (dict(dk=0), 1), (dict(dv=0), 1),
+    (dict(ws=0), 1), (dict(ws_bytes=100), 1),
+    (dict(do=DO + 8), 3), (dict(dq=DQ + 2), 3), (dict(dv=DV + 4), 3), (dict(ws=W + 8), 3),
+    (dict(dk=DQ + 64), 1),          # two outputs overlap
+    (dict(dq=DO), 1),               # an output overlaps dout
+    (dict(ws=L), 1),                # the workspace overlaps lse
+    (dict(d=96), 2), (dict(dtype=5), 2), (dict(causal=2), 1), (dict(scale=float("nan")), 1),
+    (dict(N=0), 0), (dict(B=0), 0),
+], ids=lambda x: str(x))
+def test_bwd_argument_checks(lib, kwargs, status):
+    assert call_bwd(**kwargs) == status
+
+
 def test_selftest_rejects_bad_limit_before_cuda(lib):
     assert fa.fa_selftest_wait_timeout(0) == 1
     assert fa.fa_selftest_wait_timeout(2_000_000) == 1
