@@ -93,7 +93,8 @@ fa_status_t launch(const Maps &mp, const void *o, const float *lse, const void *
         if (blocks > 65535LL * 16)
             blocks = 65535LL * 16;
         fa_bwd_dq_kernel<D, T><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(acc, static_cast<T *>(dq), N,
-                                                                                 static_cast<int>(Npad), chunks);
+                                                                                 static_cast<int>(Npad), chunks,
+                                                                                 scale);
     }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -21,11 +21,13 @@
 //                         S^T  = K_n Q_m^T           (tcgen05, TMEM)
 //                         dP^T = V_n dO_m^T          (tcgen05, TMEM)
 //                         P^T  = 2^(S^T scale log2e - L_m log2e)   (warps 0-7)
-//                         dS^T = P^T o (dP^T - D_m) scale          (warps 0-7)
+//                         dS^T = P^T o (dP^T - D_m)                (warps 0-7)
 //                         dV_n += P^T dO_m           (P^T read from TMEM)
-//                         dK_n += dS^T Q_m           (dS^T from shared memory)
-//                         dQ_m  = dS K_n             (the same shared tile, read
-//                                                     as an MN-major operand)
+//                         dK_n += dS^T Q_m           (dS^T read from TMEM)
+//                         dQ_m  = dS K_n             (dS^T also in shared memory,
+//                                                     read as an MN-major operand)
+//                       (the factor scale of dK and dQ is applied once, when
+//                       dK_n is written and when dQ is rounded);
 //                       and warps 8-11 add dQ_m into the fp32 accumulator with
 //                       TMA reduce-add (other key blocks add to the same rows).
 //   fa_bwd_dq_kernel    rounds the fp32 accumulator to dQ in the input dtype.
@@ -50,8 +52,11 @@ constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S^T @ 0 (P^T, 16-bit, over its first columns), dP^T @ 128,
-// dV @ 256, dK @ 256 + D, dQ @ 384 for D = 64; for D = 128 dQ_m takes the dP^T
-// columns, which the compute warps have finished reading when dQ_m is issued.
+// dV @ 256, dK @ 256 + D.  D = 64: dQ @ 384 and dS^T (16-bit) @ 448, so that
+// dP^T of the next query block can be computed while dK and dQ of this one
+// still read dS^T.  D = 128 (no spare columns): dS^T over the first dP^T
+// columns and dQ_m over all of them, which the compute warps have finished
+// reading when dK and dQ_m are issued; the next dP^T waits for dQ_m to be read.
 constexpr uint32_t kTmS = 0;
 constexpr uint32_t kTmDP = 128;
 constexpr uint32_t kTmDV = 256;
@@ -65,22 +70,39 @@ __host__ __device__ constexpr uint32_t col_dq()
 {
     return D == 64 ? 384u : kTmDP;
 }
-// TMEM column of K step t (queries 16t .. 16t + 15) of P^T: compute
-// warpgroup c writes the P^T of its queries [64c, 64c + 64) over S^T columns
-// [64c, 64c + 32), which it has already read.
-__host__ __device__ constexpr uint32_t tm_p_step(int t)
+template <int D>
+__host__ __device__ constexpr uint32_t col_ds()
 {
-    return kTmS + 64u * (t >> 2) + 8u * (t & 3);
+    return D == 64 ? 448u : kTmDP;
+}
+// Column distance between the two compute warpgroups' halves of a 16-bit
+// P^T / dS^T tile (each half: 64 queries, two per column = 32 columns).  Over
+// a 128-column fp32 source (P^T over S^T; dS^T over dP^T for D = 128) each
+// half sits on the source columns of its own queries: 64 apart.  In the
+// dedicated 64-column dS^T area of D = 64 the halves are adjacent: 32 apart.
+template <int D>
+__host__ __device__ constexpr uint32_t ds_half()
+{
+    return D == 64 ? 32u : 64u;
+}
+static_assert(448u + 2 * 32u <= kTmemCols && 128u + 64u + 32u <= 256u, "dS^T columns inside their area");
+// TMEM column, relative to the start of the P^T or dS^T area, of K step t
+// (queries 16t .. 16t + 15) of those 16-bit tiles, whose warpgroup halves are
+// `half` columns apart: compute warpgroup c writes the values of its queries
+// [64c, 64c + 64) to columns [half c, half c + 32).
+__host__ __device__ constexpr uint32_t tm_p_step(int t, uint32_t half)
+{
+    return half * (t >> 2) + 8u * (t & 3);
 }
 
 template <int D>
 struct Cfg {
     static constexpr int TILE = kBlk * D * 2;  // one [128, D] 16-bit tile
-    static constexpr int QST = 2;              // Q (+ L) ring
-    static constexpr int DOST = D == 64 ? 2 : 1;  // dO (+ D) ring
+    static constexpr int QST = D == 64 ? 3 : 2;   // Q (+ L) ring
+    static constexpr int DOST = D == 64 ? 3 : 1;  // dO (+ D) ring
     static constexpr int NSTG = D == 64 ? 2 : 1;  // dQ staging buffers
     static constexpr int STG_BYTES = kBlk * 32 * 4;  // [128 rows x 32 fp32], 128B-swizzled
-    static constexpr bool DQ_ALIAS = D == 128;
+    static constexpr bool DQ_ALIAS = D == 128;  // dQ (and dS^T) over the dP^T columns
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + TILE;
     static constexpr int Q_OFF = V_OFF + TILE;
@@ -253,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t q_mn = make_sdesc_sw128(sbase + C::Q_OFF, kSwAtomBytes, 1024);
             const uint64_t do_kmaj = make_sdesc_sw128(sbase + C::DO_OFF, 16, 1024);
             const uint64_t do_mn = make_sdesc_sw128(sbase + C::DO_OFF, kSwAtomBytes, 1024);
-            const uint64_t ds_kmaj = make_sdesc_sw128(sbase + C::DS_OFF, 16, 1024);
             const uint64_t ds_mn = make_sdesc_sw128(sbase + C::DS_OFF, kSwAtomBytes, 1024);
             // K step kk: 16 elements along the row (K-major: 32 bytes inside a
             // 64-column swizzle block, then the next block), or 16 rows
@@ -279,14 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_dv = [&](int s, bool acc) {  // dV += P^T dO
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 16; ++kk)
-                    umma_f16_ts(tmem + kTmDV, tmem + tm_p_step(kk), do_mn + tile(s) + mn(kk), idesc_acc,
+                    umma_f16_ts(tmem + kTmDV, tmem + kTmS + tm_p_step(kk, 64), do_mn + tile(s) + mn(kk), idesc_acc,
                                 (acc || kk > 0) ? 1u : 0u);
             };
-            auto issue_dk = [&](int s, bool acc) {  // dK += dS^T Q
+            auto issue_dk = [&](int s, bool acc) {  // dK += dS^T Q (dS^T from TMEM)
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 16; ++kk)
-                    umma_f16_ss(tmem + col_dk<D>(), ds_kmaj + kmaj(kk), q_mn + tile(s) + mn(kk), idesc_acc,
-                                (acc || kk > 0) ? 1u : 0u);
+                    umma_f16_ts(tmem + col_dk<D>(), tmem + col_ds<D>() + tm_p_step(kk, ds_half<D>()), q_mn + tile(s) + mn(kk),
+                                idesc_acc, (acc || kk > 0) ? 1u : 0u);
             };
             auto issue_dq = [&]() {  // dQ = dS K
 #pragma unroll
@@ -329,6 +350,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // the compute warps are done with D_m; dP^T and dV have read dO_m
                 umma_commit(bar(C::B_DOEMPTY + ds));
+                const int ds1 = (i + 1) % DOST;
+                if (!C::DQ_ALIAS && i + 1 < cnt) {
+                    // D = 64: dP^T of the next block first (its columns are free:
+                    // dS^T has columns of its own), so the compute warps can go on
+                    if (!(ok = wait_bounded(bar(C::B_DOFULL + ds1), ((i + 1) / DOST) & 1, abort_flag)))
+                        break;
+                    tc_fence_after();
+                    issue_dp(ds1);
+                    umma_commit(bar(C::B_DPFULL));
+                }
+                // D = 128: dK reads dS^T from the dP^T columns before dQ writes
+                // them (one thread's MMAs run in issue order)
                 issue_dk(s, i > 0);
                 if (!C::DQ_ALIAS && i > 0) {
                     if (!(ok = wait_bounded(bar(C::B_DQFREE), (i - 1) & 1, abort_flag)))
@@ -338,14 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_dq();
                 umma_commit(bar(C::B_DQFULL));
                 umma_commit(bar(C::B_QEMPTY + s));
-                if (i + 1 < cnt) {
-                    if (C::DQ_ALIAS) {
-                        // dQ_m sits in the dP^T columns: wait until it is read out
-                        if (!(ok = wait_bounded(bar(C::B_DQFREE), ph, abort_flag)))
-                            break;
-                    }
-                    const int ds1 = (i + 1) % DOST;
-                    if (!(ok = wait_bounded(bar(C::B_DOFULL + ds1), ((i + 1) / DOST) & 1, abort_flag)))
+                if (C::DQ_ALIAS && i + 1 < cnt) {
+                    // dQ_m sits in the dP^T columns: wait until it is read out
+                    if (!(ok = wait_bounded(bar(C::B_DQFREE), ph, abort_flag) &&
+                               wait_bounded(bar(C::B_DOFULL + ds1), ((i + 1) / DOST) & 1, abort_flag)))
                         break;
                     tc_fence_after();
                     issue_dp(ds1);
@@ -411,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_valid = n * kBlk + r < N;
         const uint32_t ds_row = sbase + C::DS_OFF + c * kSwAtomBytes + r * 128;
         const float2 c2 = make_float2(scale_log2, scale_log2);
-        const float2 sc = make_float2(scale, scale);
+        const uint32_t ds_tm = tmem + lane_base + col_ds<D>();
         bool ok = true;
         for (int i = 0; i < cnt; ++i) {
             const int m = m0 + i;
@@ -434,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
                     const int q = 64 * c + 32 * ch + j;
-                    const float2 l2 = *reinterpret_cast<const float2 *>(lrow + q);
+                    const float4 l4 = *reinterpret_cast<const float4 *>(lrow + (q & ~3));
+                    const float2 l2 = (q & 2) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
                     const float2 x = ffma2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])), c2,
                                            make_float2(-l2.x, -l2.y));
                     float e0 = ex2_approx(x.x);
@@ -458,8 +488,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(bar(C::B_PFULL));
 
             // ---- dS^T = P^T o (dP^T - D) scale, into shared memory ----
+            // D = 64: dK and dQ of the previous block (issued after this dP^T)
+            // must have finished reading dS^T before it is overwritten
             ok = wait_bounded(bar(C::B_DPFULL), ph, abort_flag) &&
-                 wait_bounded(bar(C::B_DOFULL + ds), (i / DOST) & 1, abort_flag);
+                 wait_bounded(bar(C::B_DOFULL + ds), (i / DOST) & 1, abort_flag) &&
+                 (C::DQ_ALIAS || i == 0 || wait_bounded(bar(C::B_DQFULL), ph ^ 1u, abort_flag));
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
@@ -473,20 +506,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
                     const int q = 64 * c + 32 * ch + j;
-                    const float2 dd = *reinterpret_cast<const float2 *>(drow + q);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(drow + (q & ~3));
+                    const float2 dd = (q & 2) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
                     const float2 p = DTypeTraits<T>::unpack(pk[16 * ch + j / 2]);
                     const float2 t = fadd2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])),
                                            make_float2(-dd.x, -dd.y));
-                    const float2 g = fmul2(fmul2(p, sc), t);
+                    // dS without the scale factor: dK and dQ apply it once at the end
+                    const float2 g = fmul2(p, t);
                     w[j / 2] = DTypeTraits<T>::pack(g.x, g.y);
                 }
-                // 16-byte chunk 4 ch + k of this row (8 queries each)
+                // dS^T into TMEM (A operand of dK) and into shared memory
+                // (MN-major A operand of dQ): 16-byte chunk 4 ch + k of this row
+                // (8 queries each)
+                tmem_st16(ds_tm + ds_half<D>() * c + 16 * ch, w);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     st_shared_v4(ds_row + ((((4 * ch + k) ^ (r & 7)) & 7) << 4), w[4 * k], w[4 * k + 1],
                                  w[4 * k + 2], w[4 * k + 3]);
             }
             fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_DSFULL));
         }
@@ -504,10 +543,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!bad) {
             tc_fence_after();
 #pragma unroll
+            // dK = scale dS^T Q (dS was kept without the scale); dV as is
+            const float mul = c == 0 ? 1.f : scale;
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 uint32_t u[32];
                 tmem_ld32(acc_tm + 32 * c4, u);
-                const float *f = reinterpret_cast<const float *>(u);
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    f[j] = __uint_as_float(u[j]) * mul;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
                     st_shared_v4(stage + sw128_offset(r, c4 * 4 + q4),
@@ -584,10 +628,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const T *__restrict__ 
     }
 }
 
-// dQ [BH, N, D] in the input dtype from the fp32 accumulator [BH, Npad, D].
+// dQ [BH, N, D] = scale x the fp32 accumulator [BH, Npad, D] (which holds
+// dS K without the scale), rounded to the input dtype.
 template <int D, typename T>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float *__restrict__ dqacc, T *__restrict__ dq,
-                                                        int N, int Npad, long long chunks)
+                                                        int N, int Npad, long long chunks, float scale)
 {
     constexpr int CPR = D / 8;  // 8-element chunks per row
     for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < chunks;
@@ -598,7 +643,9 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float *__restrict_
         const int i = static_cast<int>(row % N);
         const float4 *src = reinterpret_cast<const float4 *>(
             dqacc + (static_cast<size_t>(bh) * Npad + i) * D + part * 8);
-        const float4 a = src[0], b = src[1];
+        float4 a = src[0], b = src[1];
+        a.x *= scale, a.y *= scale, a.z *= scale, a.w *= scale;
+        b.x *= scale, b.y *= scale, b.z *= scale, b.w *= scale;
         *reinterpret_cast<uint4 *>(dq + static_cast<size_t>(row) * D + part * 8) =
             make_uint4(DTypeTraits<T>::pack(a.x, a.y), DTypeTraits<T>::pack(a.z, a.w),
                        DTypeTraits<T>::pack(b.x, b.y), DTypeTraits<T>::pack(b.z, b.w));

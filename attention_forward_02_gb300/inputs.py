@@ -33,6 +33,9 @@ WORKLOADS = {
     "d128": (2, 16, 8192, 128, "bf16", (30, 31, 32)),
     "long": (1, 8, 65536, 128, "fp16", (40, 41, 42)),
 }
+# seed of the upstream gradient dO per workload (backward pass)
+DOUT_SEEDS = {"tiny": 3, "base": 13, "sweep_b1": 33, "sweep_b2": 34, "sweep_b4": 35,
+              "sweep_b8": 53, "d128": 36, "long": 44}
 # seed of the query rows the oracle checks on the long-context workload
 LONG_ROW_SAMPLE_SEED = 43
 LONG_ROWS_PER_HEAD = 512

@@ -15,6 +15,11 @@ clocks (nvidia-smi sampled during warm-up + timed region), gpu_launches.
 --impl reference times the fp64 CPU oracle (the reference arm of this build)
 on a bounded row sample of the same workload, on the host cores.
 
+--op bwd measures the backward pass instead (fa_bwd: gradients of Q, K, V from
+the forward's O and LSE and an upstream gradient dO), FLOPs = 2.5x the
+forward's (five N x N x d products per head instead of two); its CPU legs time
+the fp64 oracle's backward on a bounded sample of heads.
+
 Multi-GPU (torchrun): each rank runs its own copy of the workload on its own
 GPU (weak scaling; attention over (batch*head, Q tile) needs no exchange);
 time = max over ranks; value = all ranks' FLOPs / that time.
@@ -34,6 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
+METRIC_BWD = "attention bwd TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -44,6 +50,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="base")
+    ap.add_argument("--op", choices=["fwd", "bwd"], default="fwd",
+                    help="fwd: the attention forward (the default step); bwd: the backward pass")
     ap.add_argument("--kernel", choices=["fa2", "fa1"], default="fa2",
                     help="fa2: the tiled FA2 forward (the product); fa1: the FA1-structured "
                          "baseline the pages compare it against")
@@ -63,6 +71,10 @@ def flops_of(meta, causal):
     return f / 2 if causal else f
 
 
+def bwd_flops_of(meta, causal):
+    return 2.5 * flops_of(meta, causal)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -73,20 +85,30 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+# Sources each kernel's translation unit compiles: a recorded DRAM figure
+# stays valid while these hash to the recorded value.
+KERNEL_SOURCES = {
+    "fa2": ("fa_fwd.cu", "fa_fwd_kernel.cuh", "fa1_fwd_kernel.cuh", "fa_common.cuh", "fa_host.h",
+            "sm100_ptx.cuh"),
+    "fa1": ("fa_fwd.cu", "fa_fwd_kernel.cuh", "fa1_fwd_kernel.cuh", "fa_common.cuh", "fa_host.h",
+            "sm100_ptx.cuh"),
+    "bwd": ("fa_bwd.cu", "fa_bwd_kernel.cuh", "fa_common.cuh", "fa_host.h", "sm100_ptx.cuh"),
+}
+
+
+def kernel_source_hash(kernel="fa2"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_02_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
 def recorded_traffic(workload, src_hash, kernel="fa2"):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, valid only while the kernel sources are the ones profiled."""
-    stem = "fa_fwd" if kernel == "fa2" else "fa1_fwd"
+    stem = {"fa2": "fa_fwd", "fa1": "fa1_fwd", "bwd": "fa_bwd"}[kernel]
     path = os.path.join(ROOT, "profiles", "%s_%s_dram.md" % (stem, workload))
     try:
         text = open(path).read()
@@ -272,6 +294,60 @@ def cpu_baseline_obj(timer, seconds, seed=99):
                                    dt)}
 
 
+class OracleBwdTimer:
+    """Times the fp64 oracle's backward (as it stands) on whole heads of the workload."""
+
+    def __init__(self, q, k, v, do, meta, variants):
+        import oracle
+        self.orc = oracle.get()
+        self.meta = meta
+        self.variants = variants
+        B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+        self.q64, self.k64, self.v64, self.do64 = (t.double().numpy().reshape(B * H, 1, N, d)
+                                                   for t in (q, k, v, do))
+        self.threads = self.orc.default_threads()
+        self.scale = d ** -0.5
+
+    def run(self, heads):
+        """heads: head indices; each variant runs them as one batch over the threads."""
+        import numpy as np
+        sel = np.asarray(heads, dtype=np.int64)
+        q, k, v, g = (x[sel].reshape(1, len(sel), self.meta["N"], self.meta["d"])
+                      for x in (self.q64, self.k64, self.v64, self.do64))
+        t0 = time.perf_counter()
+        flops = 0.0
+        one = dict(self.meta, B=1, H=len(sel))
+        for causal in self.variants:
+            self.orc.attention_bwd(q, k, v, g, self.scale, causal=causal, threads=self.threads)
+            flops += bwd_flops_of(one, causal)
+        return time.perf_counter() - t0, flops
+
+    def threads_used(self, n_heads):
+        """Threads the oracle starts for n_heads (it gives each ceil(n/threads) heads)."""
+        per = -(-n_heads // min(self.threads, n_heads))
+        return -(-n_heads // per)
+
+    def heads_for_seconds(self, seconds):
+        total = self.meta["B"] * self.meta["H"]
+        n = min(total, self.threads)
+        dt, _ = self.run(list(range(n)))
+        per = max(dt / n, 1e-9)
+        # whole rounds of `threads` heads (the oracle splits heads over threads)
+        want = max(1, int(seconds / per))
+        return max(1, min(total, want))
+
+
+def cpu_baseline_bwd_obj(timer, seconds):
+    n = timer.heads_for_seconds(seconds)
+    heads = list(range(n))
+    dt, flops = timer.run(heads)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": timer.threads_used(n),
+            "kind": "oracle",
+            "sample": "%d of %d heads of workload %s, variants %s, fp64 C oracle backward, %.1f s"
+                      % (n, timer.meta["B"] * timer.meta["H"], timer.meta["name"],
+                         "+".join("causal" if c else "noncausal" for c in timer.variants), dt)}
+
+
 # ---------------------------------------------------------------------------
 
 
@@ -293,6 +369,16 @@ def main():
               "parallelism": "dp%d (independent replicas)" % max(world, args.gpus)}
     step_flops = sum(flops_of(meta, c) for c in variants)
     config["kernel"] = args.kernel
+
+    if args.op == "bwd":
+        config["op"] = "backward (dQ, dK, dV from O, LSE and dO)"
+        config["kernel"] = "fa_bwd"
+        do = inputs.make_dout(meta["B"], meta["H"], meta["N"], meta["d"], meta["dtype"],
+                              inputs.DOUT_SEEDS.get(args.workload, 3))
+        config["inputs"] += "; dO seeded iid N(0,1) (seed %d)" % inputs.DOUT_SEEDS.get(args.workload, 3)
+        if args.impl == "reference":
+            return run_reference_bwd(args, q, k, v, do, meta, variants, config, world, rank)
+        return run_bwd(args, q, k, v, do, meta, variants, config, world, rank, local)
 
     if args.impl == "reference":
         return run_reference(args, q, k, v, meta, variants, config, step_flops, world, rank)
@@ -386,7 +472,7 @@ def main():
     dom_ms = statistics.mean(per_kernel_ms[dom])
     achieved = flops_of(meta, dom_causal) / (dom_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    src_hash = kernel_source_hash()
+    src_hash = kernel_source_hash(args.kernel)
     traffic, traffic_src = recorded_traffic(args.workload, src_hash, args.kernel)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
@@ -490,6 +576,199 @@ def run_reference(args, q, k, v, meta, variants, config, step_flops, world, rank
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def run_bwd(args, q, k, v, do, meta, variants, config, world, rank, local):
+    """The backward pass: one step = fa_bwd for each variant (inputs resident)."""
+    import torch
+    import attention_forward_02_gb300 as fa
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product has no CPU path)")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    fa.load()
+    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+    scale = d ** -0.5
+    stream = torch.cuda.current_stream(dev)
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    fwd = [fa.fa_fwd(qd, kd, vd, scale=scale, causal=c) for c in variants]  # the backward's inputs
+    grads = [tuple(torch.empty_like(qd) for _ in range(3)) for _ in variants]
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def run_one(j, causal):
+        o, lse = fwd[j]
+        dq, dk, dv = grads[j]
+        fa.fa_bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=causal, dq=dq, dk=dk, dv=dv,
+                  workspace=ws, stream=stream)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    t_load0 = time.time()
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        for j, c in enumerate(variants):
+            run_one(j, c)
+    torch.cuda.synchronize(dev)
+    st = fa.fa_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise SystemExit("device status after warm-up: %s" % fa.fa_status_str(st))
+    K = args.steps
+    nv = len(variants)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nv + 1)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(2_000_000)
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, c in enumerate(variants):
+            run_one(j, c)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    sampler.mark_load(t_load0, time.time())
+    st = fa.fa_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise SystemExit("device status after timed region: %s" % fa.fa_status_str(st))
+    step_flops = sum(bwd_flops_of(meta, c) for c in variants)
+    step_ms = [ev[i][0].elapsed_time(ev[i][nv]) for i in range(K)]
+    per_call_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)] for j in range(nv)]
+    total_ms = max_over_ranks(dist, sum(step_ms), dev)
+    value = sum_over_ranks(dist, step_flops * K, dev) / (total_ms / 1e3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e_bwd(fa, torch, q, k, v, do, meta, variants, dev, stream, scale, step_flops,
+                          max(3, min(K, 20)), dist)
+    clocks = sampler.stop()
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    dom = variants.index(False) if False in variants else 0
+    dom_ms = statistics.mean(per_call_ms[dom])
+    achieved = bwd_flops_of(meta, variants[dom]) / (dom_ms / 1e3) / 1e12
+    traffic, _ = recorded_traffic(args.workload, kernel_source_hash("bwd"), "bwd")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "fa_bwd_kernel<%d,%s,%s>" % (d, "causal" if variants[dom] else "noncausal",
+                                                       meta["dtype"]),
+                "timed": "the whole fa_bwd call (row-term kernel + main kernel + dQ rounding); "
+                         "the main kernel's own rate is higher by its share of the call",
+                "peak_source": "%s bf16_tflops (burst; fp16 dense rate equals bf16)" % peak_src,
+                "launch_ms": dom_ms,
+                "algorithmic_flops_per_launch": bwd_flops_of(meta, variants[dom]),
+                "variants_tflops": {("causal" if c else "noncausal"):
+                                    bwd_flops_of(meta, c) / (statistics.mean(per_call_ms[j]) / 1e3)
+                                    / 1e12 for j, c in enumerate(variants)}}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_bwd_obj(OracleBwdTimer(q, k, v, do, meta, variants), args.cpu_seconds)
+    if rank == 0:
+        line = {"metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "pct_of_peak": 100.0 * value / peak, "dtype": meta["dtype"], "data": "synthetic",
+                "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clocks, "gpu_launches": K * nv * 3, "wall_s_timed": t_wall}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e_bwd(fa, torch, q, k, v, do, meta, variants, dev, stream, scale, step_flops, steps, dist):
+    """Backward through the public API from pinned host buffers: per step the
+    H2D copy of q, k, v, o, lse, dO (o, lse made once by the forward), the
+    backward, and the D2H copy of dq, dk, dv, for each variant."""
+    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    dq_, dk_, dv_, ddo = (torch.empty_like(hq, device=dev) for _ in range(4))
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    host_fwd = []
+    for c in variants:
+        o, l = fa.fa_fwd(hq.to(dev), hk.to(dev), hv.to(dev), scale=scale, causal=c)
+        host_fwd.append((o.cpu().pin_memory(), l.cpu().pin_memory()))
+    od = torch.empty_like(dq_)
+    ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    outs_h = [tuple(torch.empty_like(hq).pin_memory() for _ in range(3)) for _ in variants]
+    grads_d = tuple(torch.empty_like(dq_) for _ in range(3))
+    h2d = len(variants) * (5 * hq.numel() * hq.element_size() + ld.numel() * 4)
+    d2h = len(variants) * 3 * hq.numel() * hq.element_size()
+
+    def one():
+        for (ho, hl), (hdq, hdk, hdv), c in zip(host_fwd, outs_h, variants):
+            dq_.copy_(hq, non_blocking=True)
+            dk_.copy_(hk, non_blocking=True)
+            dv_.copy_(hv, non_blocking=True)
+            ddo.copy_(hdo, non_blocking=True)
+            od.copy_(ho, non_blocking=True)
+            ld.copy_(hl, non_blocking=True)
+            fa.fa_bwd(dq_, dk_, dv_, od, ld, ddo, scale=scale, causal=c, dq=grads_d[0],
+                      dk=grads_d[1], dv=grads_d[2], workspace=ws, stream=stream)
+            hdq.copy_(grads_d[0], non_blocking=True)
+            hdk.copy_(grads_d[1], non_blocking=True)
+            hdv.copy_(grads_d[2], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    flops = step_flops * steps
+    if dist is not None:
+        ms = max_over_ranks(dist, ms, dev)
+        flops = sum_over_ranks(dist, flops, dev)
+    return {"value": flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+
+
+def run_reference_bwd(args, q, k, v, do, meta, variants, config, world, rank):
+    """The reference arm for the backward: the fp64 oracle's backward on host cores."""
+    if rank != 0:
+        return
+    timer = OracleBwdTimer(q, k, v, do, meta, variants)
+    budget = max(0.5, args.ref_seconds)
+    n_steps = args.steps + max(args.warmup, 0)
+    heads = timer.heads_for_seconds(budget / max(n_steps, 1))
+    total = meta["B"] * meta["H"]
+    for i in range(max(args.warmup, 0)):
+        timer.run([(i * heads + h) % total for h in range(heads)])
+    tot_t, tot_f = 0.0, 0.0
+    for i in range(args.steps):
+        dt, fl = timer.run([((i + args.warmup) * heads + h) % total for h in range(heads)])
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = ("each step: %d of %d heads of %s, variants %s, fp64 C oracle backward"
+              % (heads, total, args.workload, "+".join(config["variants"])))
+    print(json.dumps({"impl": "reference", "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s",
+                      "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": config,
+                      "cpu_baseline": {"value": value, "unit": "TFLOP/s",
+                                       "cores": timer.threads_used(heads), "kind": "oracle",
+                                       "sample": sample},
+                      "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}), flush=True)
 
 
 if __name__ == "__main__":
