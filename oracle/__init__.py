@@ -61,6 +61,11 @@ class Oracle:
         L.oracle_attention_bwd.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
                                            ctypes.c_long, ctypes.c_double, ctypes.c_int,
                                            _dp, _dp, _dp, ctypes.c_int]
+        L.oracle_attention_bwd_rows.restype = ctypes.c_int
+        L.oracle_attention_bwd_rows.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                                ctypes.c_long, ctypes.c_double, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_long), ctypes.c_long, _dp,
+                                                ctypes.c_int]
         L.oracle_abi_version.restype = ctypes.c_int
 
     # -- helpers -----------------------------------------------------------
@@ -144,6 +149,23 @@ class Oracle:
         if st != 0:
             raise OracleError("oracle_attention_bwd returned %d" % st)
         return dq, dk, dv
+
+    def attention_bwd_rows(self, q, k, v, g, rows, scale, causal=False, threads=None):
+        """dq of the listed query rows; rows: int array [n, 2] of (flattened
+        head, query index).  Returns [n, d] fp64."""
+        q, k, v, g = self._f64(q), self._f64(k), self._f64(v), self._f64(g)
+        if q.ndim != 4 or any(t.shape != q.shape for t in (k, v, g)):
+            raise OracleError("q, k, v, g must share a [B,H,N,d] shape")
+        B, H, N, d = q.shape
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 2))
+        out = np.empty((len(rows), d))
+        st = self._lib.oracle_attention_bwd_rows(
+            self._ptr(q), self._ptr(k), self._ptr(v), self._ptr(g), B * H, N, d, float(scale),
+            int(bool(causal)), rows.ctypes.data_as(ctypes.POINTER(ctypes.c_long)), len(rows),
+            self._ptr(out), threads or self.default_threads())
+        if st != 0:
+            raise OracleError("oracle_attention_bwd_rows returned %d" % st)
+        return out
 
     # -- online recurrence -------------------------------------------------
     def online_row(self, s, v, blocks):

@@ -39,7 +39,8 @@
  *    (section 3.6.5) and the block-order independence the page claims.
  *
  *  - oracle_attention_bwd: the gradients of the plain definition (softmax
- *    Jacobian), for the backward pass.
+ *    Jacobian), for the backward pass; oracle_attention_bwd_rows: dq of
+ *    listed query rows only (O(N d) each, for full-size samples).
  *
  * Every function here is pinned by tests under tests/ (worked example,
  * exercise, closed forms, invariants, finite differences, source mutations).
@@ -369,82 +370,116 @@ int oracle_online_row(const double *s, const double *v, long n, long d,
  * Rows are processed one at a time (two passes over the keys, like the
  * forward), so memory is O(N d) per head.
  */
-static void backward_head(const double *q, const double *k, const double *v, const double *g,
-                          long n, long d, double scale, int causal, double *s, double *dp,
-                          double *dq, double *dk, double *dv)
+/* One query row i of one head over its n_keys allowed keys: leaves
+ * s[j] = p_ij and dp[j] = <g_i, v_j>, writes dq_i, and returns
+ * sum_j p_ij dp_ij (the row's D term of the softmax Jacobian). */
+static double backward_row(const double *q, const double *k, const double *v, const double *g,
+                           long i, long n_keys, long d, double scale, double *s, double *dp,
+                           double *dq_i)
 {
-    for (long x = 0; x < n * d; ++x) {
-        dq[x] = 0.0;
-        dk[x] = 0.0;
-        dv[x] = 0.0;
+    scores_row(q, k, i, n_keys, d, scale, s);
+    double m = -INFINITY;
+    for (long j = 0; j < n_keys; ++j)
+        if (s[j] > m)
+            m = s[j];
+    double row_sum = 0.0;
+    for (long j = 0; j < n_keys; ++j)
+        row_sum += exp(s[j] - m);
+    /* s <- p_ij, dp <- <g_i, v_j> */
+    double pdp = 0.0;
+    for (long j = 0; j < n_keys; ++j) {
+        s[j] = exp(s[j] - m) / row_sum;
+        double dot = 0.0;
+        for (long c = 0; c < d; ++c)
+            dot += g[i * d + c] * v[j * d + c];
+        dp[j] = dot;
+        pdp += s[j] * dot;
     }
-    for (long i = 0; i < n; ++i) {
+    for (long c = 0; c < d; ++c)
+        dq_i[c] = 0.0;
+    for (long j = 0; j < n_keys; ++j) {
+        const double ds_ij = s[j] * (dp[j] - pdp);
+        for (long c = 0; c < d; ++c)
+            dq_i[c] += scale * ds_ij * k[j * d + c];
+    }
+    return pdp;
+}
+
+/* Query rows [i0, i1) of one head: their dq rows are written, and their
+ * contributions are added into dk and dv. */
+static void backward_rows(const double *q, const double *k, const double *v, const double *g,
+                          long n, long d, double scale, int causal, long i0, long i1, double *s,
+                          double *dp, double *dq, double *dk, double *dv)
+{
+    for (long i = i0; i < i1; ++i) {
         long n_keys = allowed_keys(i, n, causal);
-        scores_row(q, k, i, n_keys, d, scale, s);
-        double m = -INFINITY;
-        for (long j = 0; j < n_keys; ++j)
-            if (s[j] > m)
-                m = s[j];
-        double row_sum = 0.0;
-        for (long j = 0; j < n_keys; ++j)
-            row_sum += exp(s[j] - m);
-        /* s <- p_ij, dp <- <g_i, v_j> */
-        double pdp = 0.0;
-        for (long j = 0; j < n_keys; ++j) {
-            s[j] = exp(s[j] - m) / row_sum;
-            double dot = 0.0;
-            for (long c = 0; c < d; ++c)
-                dot += g[i * d + c] * v[j * d + c];
-            dp[j] = dot;
-            pdp += s[j] * dot;
-        }
+        double pdp = backward_row(q, k, v, g, i, n_keys, d, scale, s, dp, dq + i * d);
         for (long j = 0; j < n_keys; ++j) {
             double ds = s[j] * (dp[j] - pdp);
             for (long c = 0; c < d; ++c) {
                 dv[j * d + c] += s[j] * g[i * d + c];
-                dq[i * d + c] += scale * ds * k[j * d + c];
                 dk[j * d + c] += scale * ds * q[i * d + c];
             }
         }
     }
 }
 
+/* A share of the work: query rows [i0, i1) of head `head`.  dk and dv point
+ * at the head's outputs when one job covers the whole head, else at private
+ * accumulators that are summed afterwards in job order. */
 typedef struct {
     const double *q, *k, *v, *g;
     long n, d;
     double scale;
     int causal;
+    long head, i0, i1;
     double *dq, *dk, *dv;
-    long begin, end;
     int status;
-} head_job;
+} rows_job;
 
-static void *head_worker(void *arg)
+static void run_rows_job(rows_job *jb)
 {
-    head_job *job = (head_job *)arg;
-    double *s = (double *)malloc((size_t)(job->n > 0 ? job->n : 1) * sizeof(double));
-    double *dp = (double *)malloc((size_t)(job->n > 0 ? job->n : 1) * sizeof(double));
+    double *s = (double *)malloc((size_t)(jb->n > 0 ? jb->n : 1) * sizeof(double));
+    double *dp = (double *)malloc((size_t)(jb->n > 0 ? jb->n : 1) * sizeof(double));
     if (!s || !dp) {
         free(s);
         free(dp);
-        job->status = ORACLE_ENOMEM;
-        return NULL;
+        jb->status = ORACLE_ENOMEM;
+        return;
     }
-    long he = job->n * job->d;
-    for (long bh = job->begin; bh < job->end; ++bh)
-        backward_head(job->q + bh * he, job->k + bh * he, job->v + bh * he, job->g + bh * he,
-                      job->n, job->d, job->scale, job->causal, s, dp, job->dq + bh * he,
-                      job->dk + bh * he, job->dv + bh * he);
+    long he = jb->n * jb->d;
+    for (long x = 0; x < he; ++x) {
+        jb->dk[x] = 0.0;
+        jb->dv[x] = 0.0;
+    }
+    backward_rows(jb->q + jb->head * he, jb->k + jb->head * he, jb->v + jb->head * he,
+                  jb->g + jb->head * he, jb->n, jb->d, jb->scale, jb->causal, jb->i0, jb->i1, s, dp,
+                  jb->dq + jb->head * he, jb->dk, jb->dv);
     free(s);
     free(dp);
-    job->status = ORACLE_OK;
+    jb->status = ORACLE_OK;
+}
+
+typedef struct {
+    rows_job *jobs;
+    long begin, end;
+} job_range;
+
+static void *jobs_worker(void *arg)
+{
+    job_range *r = (job_range *)arg;
+    for (long t = r->begin; t < r->end; ++t)
+        run_rows_job(&r->jobs[t]);
     return NULL;
 }
 
 /*
  * oracle_attention_bwd: gradients dq, dk, dv ([BH, N, d] fp64) of
  * L = sum(o * g) for the plain definition, given q, k, v and g = dL/do
- * ([BH, N, d] fp64).  Threads split the heads.
+ * ([BH, N, d] fp64).  The work is split into (head, query-row range) jobs:
+ * one job per head when there are at least as many heads as threads, else
+ * each head's rows are split so that every thread has work; split heads sum
+ * their jobs' dk, dv in job order.
  */
 int oracle_attention_bwd(const double *q, const double *k, const double *v, const double *g,
                          long BH, long N, long d, double scale, int causal, double *dq,
@@ -458,42 +493,166 @@ int oracle_attention_bwd(const double *q, const double *k, const double *v, cons
         return ORACLE_EINVAL;
     if (nthreads <= 0)
         nthreads = 1;
-    if (nthreads > BH)
-        nthreads = (int)BH;
-    head_job *jobs = (head_job *)calloc((size_t)nthreads, sizeof(head_job));
+    long splits = nthreads > BH ? nthreads / BH : 1;
+    if (splits > N)
+        splits = N;
+    const long njobs = BH * splits;
+    const long he = N * d;
+    rows_job *jobs = (rows_job *)calloc((size_t)njobs, sizeof(rows_job));
+    double *priv = splits > 1 ? (double *)malloc((size_t)njobs * 2 * (size_t)he * sizeof(double)) : NULL;
+    if (!jobs || (splits > 1 && !priv)) {
+        free(jobs);
+        free(priv);
+        return ORACLE_ENOMEM;
+    }
+    const long rows_per = (N + splits - 1) / splits;
+    for (long h = 0; h < BH; ++h) {
+        for (long sp = 0; sp < splits; ++sp) {
+            rows_job *jb = &jobs[h * splits + sp];
+            jb->q = q; jb->k = k; jb->v = v; jb->g = g; jb->n = N; jb->d = d;
+            jb->scale = scale; jb->causal = causal; jb->head = h; jb->dq = dq;
+            jb->i0 = sp * rows_per < N ? sp * rows_per : N;
+            jb->i1 = (sp + 1) * rows_per < N ? (sp + 1) * rows_per : N;
+            if (splits > 1) {
+                jb->dk = priv + (size_t)(h * splits + sp) * 2 * (size_t)he;
+                jb->dv = jb->dk + he;
+            } else {
+                jb->dk = dk + h * he;
+                jb->dv = dv + h * he;
+            }
+            jb->status = ORACLE_OK;
+        }
+    }
+    int nt = nthreads < njobs ? nthreads : (int)njobs;
+    job_range *ranges = (job_range *)calloc((size_t)nt, sizeof(job_range));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nt, sizeof(pthread_t));
+    unsigned char *spawned = (unsigned char *)calloc((size_t)nt, 1);
+    if (!ranges || !tids || !spawned) {
+        free(ranges); free(tids); free(spawned); free(jobs); free(priv);
+        return ORACLE_ENOMEM;
+    }
+    const long per = (njobs + nt - 1) / nt;
+    for (int t = 0; t < nt; ++t) {
+        ranges[t].jobs = jobs;
+        ranges[t].begin = t * per < njobs ? t * per : njobs;
+        ranges[t].end = (t + 1) * per < njobs ? (t + 1) * per : njobs;
+        if (t < nt - 1 && pthread_create(&tids[t], NULL, jobs_worker, &ranges[t]) == 0)
+            spawned[t] = 1;
+        else
+            jobs_worker(&ranges[t]);
+    }
+    int status = ORACLE_OK;
+    for (int t = 0; t < nt; ++t)
+        if (spawned[t])
+            pthread_join(tids[t], NULL);
+    for (long x = 0; x < njobs; ++x)
+        if (jobs[x].status != ORACLE_OK)
+            status = jobs[x].status;
+    if (status == ORACLE_OK && splits > 1) {
+        for (long h = 0; h < BH; ++h) {
+            double *dkh = dk + h * he, *dvh = dv + h * he;
+            for (long x = 0; x < he; ++x) {
+                dkh[x] = 0.0;
+                dvh[x] = 0.0;
+            }
+            for (long sp = 0; sp < splits; ++sp) {
+                const rows_job *jb = &jobs[h * splits + sp];
+                for (long x = 0; x < he; ++x) {
+                    dkh[x] += jb->dk[x];
+                    dvh[x] += jb->dv[x];
+                }
+            }
+        }
+    }
+    free(ranges); free(tids); free(spawned); free(jobs); free(priv);
+    return status;
+}
+
+/*
+ * oracle_attention_bwd_rows: dq for the listed query rows only (rows[2r] =
+ * flattened head, rows[2r+1] = query index), into dq_out [nrows, d].  One
+ * row needs only its own softmax, so each costs O(N d).  Threads split the
+ * rows.
+ */
+typedef struct {
+    const double *q, *k, *v, *g;
+    long N, d;
+    double scale;
+    int causal;
+    const long *rows;
+    double *out;
+    long begin, end;
+    int status;
+} dq_rows_job;
+
+static void *dq_rows_worker(void *arg)
+{
+    dq_rows_job *jb = (dq_rows_job *)arg;
+    double *s = (double *)malloc((size_t)jb->N * sizeof(double));
+    double *dp = (double *)malloc((size_t)jb->N * sizeof(double));
+    if (!s || !dp) {
+        free(s);
+        free(dp);
+        jb->status = ORACLE_ENOMEM;
+        return NULL;
+    }
+    const long he = jb->N * jb->d;
+    for (long r = jb->begin; r < jb->end; ++r) {
+        const long bh = jb->rows[2 * r], i = jb->rows[2 * r + 1];
+        backward_row(jb->q + bh * he, jb->k + bh * he, jb->v + bh * he, jb->g + bh * he, i,
+                     allowed_keys(i, jb->N, jb->causal), jb->d, jb->scale, s, dp, jb->out + r * jb->d);
+    }
+    free(s);
+    free(dp);
+    jb->status = ORACLE_OK;
+    return NULL;
+}
+
+int oracle_attention_bwd_rows(const double *q, const double *k, const double *v, const double *g,
+                              long BH, long N, long d, double scale, int causal, const long *rows,
+                              long nrows, double *dq_out, int nthreads)
+{
+    if (BH < 0 || N < 0 || d < 1 || nrows < 0 || (causal != 0 && causal != 1))
+        return ORACLE_EINVAL;
+    if (nrows == 0)
+        return ORACLE_OK;
+    if (!q || !k || !v || !g || !rows || !dq_out || N == 0)
+        return ORACLE_EINVAL;
+    for (long r = 0; r < nrows; ++r)
+        if (rows[2 * r] < 0 || rows[2 * r] >= BH || rows[2 * r + 1] < 0 || rows[2 * r + 1] >= N)
+            return ORACLE_EINVAL;
+    if (nthreads <= 0)
+        nthreads = 1;
+    if (nthreads > nrows)
+        nthreads = (int)nrows;
+    dq_rows_job *jobs = (dq_rows_job *)calloc((size_t)nthreads, sizeof(dq_rows_job));
     pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     unsigned char *spawned = (unsigned char *)calloc((size_t)nthreads, 1);
     if (!jobs || !tids || !spawned) {
-        free(jobs);
-        free(tids);
-        free(spawned);
+        free(jobs); free(tids); free(spawned);
         return ORACLE_ENOMEM;
     }
-    long per = (BH + nthreads - 1) / nthreads;
-    int status = ORACLE_OK;
+    const long per = (nrows + nthreads - 1) / nthreads;
     for (int t = 0; t < nthreads; ++t) {
-        head_job *hj = &jobs[t];
-        hj->q = q; hj->k = k; hj->v = v; hj->g = g; hj->n = N; hj->d = d;
-        hj->scale = scale; hj->causal = causal; hj->dq = dq; hj->dk = dk; hj->dv = dv;
-        hj->begin = t * per;
-        hj->end = (t + 1) * per < BH ? (t + 1) * per : BH;
-        hj->status = ORACLE_OK;
-        if (hj->begin >= hj->end)
-            continue;
-        if (t < nthreads - 1 && pthread_create(&tids[t], NULL, head_worker, hj) == 0)
+        dq_rows_job *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v; jb->g = g; jb->N = N; jb->d = d; jb->scale = scale;
+        jb->causal = causal; jb->rows = rows; jb->out = dq_out;
+        jb->begin = t * per < nrows ? t * per : nrows;
+        jb->end = (t + 1) * per < nrows ? (t + 1) * per : nrows;
+        jb->status = ORACLE_OK;
+        if (t < nthreads - 1 && pthread_create(&tids[t], NULL, dq_rows_worker, jb) == 0)
             spawned[t] = 1;
         else
-            head_worker(hj);
+            dq_rows_worker(jb);
     }
+    int status = ORACLE_OK;
     for (int t = 0; t < nthreads; ++t) {
         if (spawned[t])
             pthread_join(tids[t], NULL);
         if (jobs[t].status != ORACLE_OK)
             status = jobs[t].status;
     }
-    free(spawned);
-    free(jobs);
-    free(tids);
+    free(jobs); free(tids); free(spawned);
     return status;
 }
 

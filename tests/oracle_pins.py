@@ -428,6 +428,23 @@ def pin_bwd_causal_first_row(orc):
     _close(dv[0, 0, 5], p_last * g[0, 0, 5], 1e-14, "causal dv of the last key")
 
 
+def pin_bwd_row_split_matches_whole_heads(orc):
+    """Splitting a head's query rows over threads (private dk, dv summed in
+    order) gives the gradients of the one-job-per-head run, up to rounding
+    order; the dq-rows entry point gives the same dq rows exactly."""
+    rng = np.random.default_rng(4545)
+    q, k, v, g = (rng.standard_normal((1, 2, 45, 6)) for _ in range(4))
+    for causal in (False, True):
+        whole = orc.attention_bwd(q, k, v, g, 0.35, causal=causal, threads=1)
+        split = orc.attention_bwd(q, k, v, g, 0.35, causal=causal, threads=7)
+        for name, a, b in zip(("dq", "dk", "dv"), whole, split):
+            _close(b, a, 1e-12, "%s split vs whole (causal=%d)" % (name, causal))
+        rows = np.array([[0, 0], [1, 44], [1, 3], [0, 22], [1, 21]])
+        dq_rows = orc.attention_bwd_rows(q, k, v, g, rows, 0.35, causal=causal, threads=3)
+        _close(dq_rows, whole[0].reshape(2, 45, 6)[rows[:, 0], rows[:, 1]], 0.0,
+               "dq rows vs whole (causal=%d)" % causal)
+
+
 PINS = [
     pin_worked_example_full,
     pin_worked_example_online,
@@ -448,4 +465,5 @@ PINS = [
     pin_bwd_sum_rules,
     pin_bwd_value_shift,
     pin_bwd_causal_first_row,
+    pin_bwd_row_split_matches_whole_heads,
 ]

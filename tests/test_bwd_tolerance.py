@@ -59,3 +59,35 @@ def test_planted_error_fails(orc, name):
     out[idx] = t.to(q.dtype)
     with pytest.raises(AssertionError):
         check_bwd(orc, q, k, v, do, 0.125, False, out, "planted %s" % name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dv_identity_holds_for_the_emulation(causal):
+    """The full-size dV identity passes on the emulated kernel and fails when
+    one dV element is off by 0.5."""
+    from bwd_util import check_dv_identity
+    q, k, v = inputs.make_qkv(1, 2, 300, 64, "fp16", (21, 22, 23))
+    do = inputs.make_dout(1, 2, 300, 64, "fp16", 24)
+    o, lse, dq, dk, dv = emulate(q, k, v, do, 0.125, causal)
+    assert check_dv_identity(do, dv, "emulated") < 0.5
+    bad = dv.float().clone()
+    bad[0, 1, 7, 3] += 0.5
+    with pytest.raises(AssertionError):
+        check_dv_identity(do, bad.to(dv.dtype), "planted dv")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dq_rows_check_on_the_emulation(orc, causal):
+    """The sampled-row dQ check passes on the emulated kernel, and fails on a
+    planted error of a quarter of the row's largest entry (the bf16 bound is a
+    worst case over the row's cancelling terms, near 15 % of |dQ| here)."""
+    from bwd_util import check_dq_rows
+    q, k, v = inputs.make_qkv(1, 2, 260, 64, "bf16", (31, 32, 33))
+    do = inputs.make_dout(1, 2, 260, 64, "bf16", 34)
+    o, lse, dq, dk, dv = emulate(q, k, v, do, 0.125, causal)
+    rows = np.array([[0, 0], [0, 129], [1, 259], [1, 64]])
+    assert check_dq_rows(orc, q, k, v, do, o, lse, dq, rows, 0.125, causal, "emulated") < 0.5
+    bad = dq.float().clone()
+    bad[0, 1, 259, 7] += 0.25 * float(bad[0, 1, 259].abs().max())
+    with pytest.raises(AssertionError):
+        check_dq_rows(orc, q, k, v, do, o, lse, bad.to(dq.dtype), rows, 0.125, causal, "planted")

@@ -6,7 +6,9 @@ import torch
 
 import oracle
 from attention_forward_02_gb300 import inputs
-from bwd_util import check_bwd, run_gpu_fwd_bwd
+import numpy as np
+
+from bwd_util import check_bwd, check_bwd_heads, check_dq_rows, check_dv_identity, run_gpu_fwd_bwd
 
 pytestmark = pytest.mark.gpu
 
@@ -52,3 +54,68 @@ def test_many_heads(orc, causal):
 def test_stress_scores(orc, causal):
     # Q x 8: scaled scores with standard deviation about 8 (peaked softmax rows)
     _case(orc, 1, 2, 640, 128, "bf16", causal, 7200, q_scale=8.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_base_sampled_heads(orc, causal):
+    """Full base workload (B=4 H=32 N=2048 d=64 fp16) on the GPU; three heads
+    compared element by element with the oracle."""
+    q, k, v, meta = inputs.make_workload("base")
+    do = inputs.make_dout(meta["B"], meta["H"], meta["N"], meta["d"], meta["dtype"],
+                          inputs.DOUT_SEEDS["base"])
+    gpu = run_gpu_fwd_bwd(q, k, v, do, 0.125, causal)
+    check_bwd_heads(orc, q, k, v, do, 0.125, causal, gpu, [0, 77, 127],
+                    "bwd base heads causal=%s" % causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d128_one_head(orc, causal):
+    """Full d128 workload (B=2 H=16 N=8192 d=128 bf16) on the GPU; one whole
+    head (8192 x 8192 scores) compared element by element with the oracle."""
+    q, k, v, meta = inputs.make_workload("d128")
+    do = inputs.make_dout(meta["B"], meta["H"], meta["N"], meta["d"], meta["dtype"],
+                          inputs.DOUT_SEEDS["d128"])
+    scale = meta["d"] ** -0.5
+    gpu = run_gpu_fwd_bwd(q, k, v, do, scale, causal)
+    check_bwd_heads(orc, q, k, v, do, scale, causal, gpu, [21], "bwd d128 head 21 causal=%s" % causal)
+
+
+@pytest.mark.parametrize("name", ["base", "d128", "long"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_size_dq_rows(orc, name, causal):
+    """The bench workloads at full size: sampled dQ rows (seeded, plus tile
+    edges and the first and last rows) against the oracle's dQ rows."""
+    q, k, v, meta = inputs.make_workload(name)
+    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+    do = inputs.make_dout(B, H, N, d, meta["dtype"], inputs.DOUT_SEEDS[name])
+    scale = d ** -0.5
+    o, lse, dq, dk, dv = run_gpu_fwd_bwd(q, k, v, do, scale, causal)
+    rng = np.random.default_rng(808)
+    heads = rng.choice(B * H, size=min(4, B * H), replace=False)
+    rows = [(h, i) for h in heads for i in (0, 127, 128, N // 2, N - 1)]
+    rows += [(int(rng.integers(B * H)), int(rng.integers(N))) for _ in range(24)]
+    check_dq_rows(orc, q, k, v, do, o, lse, dq, np.array(rows), scale, causal,
+                  "bwd %s dq rows causal=%s" % (name, causal))
+
+
+@pytest.mark.parametrize("name", ["base", "d128", "long"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_size_dv_identity(name, causal):
+    """The bench workloads at full size, in the launch configuration bench.py
+    times: every gradient finite, and sum_j dV_j = sum_i dO_i per head."""
+    import attention_forward_02_gb300 as fa
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    q, k, v, meta = inputs.make_workload(name)
+    do = inputs.make_dout(meta["B"], meta["H"], meta["N"], meta["d"], meta["dtype"],
+                          inputs.DOUT_SEEDS[name])
+    dev = torch.device("cuda:0")
+    q, k, v, do = (t.to(dev) for t in (q, k, v, do))
+    scale = meta["d"] ** -0.5
+    o, lse = fa.fa_fwd(q, k, v, scale=scale, causal=causal)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, scale=scale, causal=causal)
+    st = fa.fa_last_device_status(torch.cuda.current_stream(dev).cuda_stream)
+    assert st == 0, fa.fa_status_str(st)
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    check_dv_identity(do, dv, "bwd %s causal=%s" % (name, causal))

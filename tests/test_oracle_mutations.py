@@ -13,8 +13,8 @@ from oracle_pins import PINS
 # (name, text in attention_oracle.c, replacement)
 MUTATIONS = [
     ("dropped_scale", "s[j] = scale * dot;", "s[j] = dot;"),
-    ("dropped_feature", "for (long c = 0; c < d; ++c)\n            dot +=",
-     "for (long c = 1; c < d; ++c)\n            dot +="),
+    ("dropped_feature", "for (long c = 0; c < d; ++c)\n            dot += q[",
+     "for (long c = 1; c < d; ++c)\n            dot += q["),
     ("transposed_qk", "dot += q[i * d + c] * k[j * d + c];", "dot += q[j * d + c] * k[i * d + c];"),
     ("causal_excludes_diagonal", "return i + 1;", "return i;"),
     ("causal_off", "    if (causal)\n        return i + 1;", "    if (0)\n        return i + 1;"),
@@ -36,19 +36,21 @@ MUTATIONS = [
     ("online_no_max_shift", "pv += exp(s[j] - m_new) * v[j * d + c];", "pv += exp(s[j]) * v[j * d + c];"),
     ("online_no_final_normalise", "o_out[c] = acc[c] / l;", "o_out[c] = acc[c];"),
     ("row_slice_off_by_one", "jb->begin = t * per;", "jb->begin = t * per + (t > 0);"),
-    ("bwd_head_slice_off_by_one", "hj->begin = t * per;", "hj->begin = t * per + (t > 0);"),
+    ("bwd_row_split_off_by_one", "jb->i0 = sp * rows_per < N ? sp * rows_per : N;",
+     "jb->i0 = sp * rows_per + (sp > 0) < N ? sp * rows_per + (sp > 0) : N;"),
+    ("bwd_split_sum_first_job_only", "const rows_job *jb = &jobs[h * splits + sp];",
+     "const rows_job *jb = &jobs[h * splits];"),
+    ("bwd_rows_ignore_causal", "allowed_keys(i, jb->N, jb->causal)", "allowed_keys(i, jb->N, 0)"),
     ("bwd_dv_uses_ds", "dv[j * d + c] += s[j] * g[i * d + c];", "dv[j * d + c] += ds * g[i * d + c];"),
     ("bwd_ds_not_centred", "double ds = s[j] * (dp[j] - pdp);", "double ds = s[j] * dp[j];"),
     ("bwd_ds_sign", "double ds = s[j] * (dp[j] - pdp);", "double ds = s[j] * (pdp - dp[j]);"),
-    ("bwd_dq_no_scale", "dq[i * d + c] += scale * ds * k[j * d + c];",
-     "dq[i * d + c] += ds * k[j * d + c];"),
     ("bwd_dk_uses_k", "dk[j * d + c] += scale * ds * q[i * d + c];",
      "dk[j * d + c] += scale * ds * k[j * d + c];"),
     ("bwd_dp_transposed", "dot += g[i * d + c] * v[j * d + c];", "dot += g[j * d + c] * v[i * d + c];"),
     ("bwd_p_not_normalised", "s[j] = exp(s[j] - m) / row_sum;", "s[j] = exp(s[j] - m);"),
     ("bwd_no_max_shift", "row_sum += exp(s[j] - m);", "row_sum += exp(s[j]);"),
-    ("bwd_head_offset_dropped", "job->n, job->d, job->scale, job->causal, s, dp, job->dq + bh * he,",
-     "job->n, job->d, job->scale, job->causal, s, dp, job->dq,"),
+    ("bwd_head_offset_dropped", "jb->dq + jb->head * he, jb->dk, jb->dv);", "jb->dq, jb->dk, jb->dv);"),
+    ("bwd_dq_row_no_scale", "dq_i[c] += scale * ds_ij * k[j * d + c];", "dq_i[c] += ds_ij * k[j * d + c];"),
 ]
 
 
