@@ -66,6 +66,10 @@ class Oracle:
                                                 ctypes.c_long, ctypes.c_double, ctypes.c_int,
                                                 ctypes.POINTER(ctypes.c_long), ctypes.c_long, _dp,
                                                 ctypes.c_int]
+        L.oracle_attention_decode.restype = ctypes.c_int
+        L.oracle_attention_decode.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                              ctypes.c_long, ctypes.c_long, ctypes.c_double,
+                                              ctypes.c_int, _dp, _dp, ctypes.c_int]
         L.oracle_abi_version.restype = ctypes.c_int
 
     # -- helpers -----------------------------------------------------------
@@ -132,6 +136,25 @@ class Oracle:
         if st != 0:
             raise OracleError("oracle_scores_row returned %d" % st)
         return s[: n.value].copy()
+
+    def attention_decode(self, q, k, v, scale, causal=False, threads=None):
+        """Nq queries q [B,H,Nq,d] against Nk >= Nq keys k, v [B,H,Nk,d];
+        causal aligns the queries with the end of the keys.  Returns
+        (o [B,H,Nq,d], lse [B,H,Nq]) fp64."""
+        q, k, v = self._f64(q), self._f64(k), self._f64(v)
+        if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] \
+                or q.shape[3] != k.shape[3]:
+            raise OracleError("q [B,H,Nq,d], k and v [B,H,Nk,d] expected")
+        B, H, Nq, d = q.shape
+        Nk = k.shape[2]
+        o = np.empty_like(q)
+        lse = np.empty((B, H, Nq))
+        st = self._lib.oracle_attention_decode(self._ptr(q), self._ptr(k), self._ptr(v), B * H, Nq,
+                                               Nk, d, float(scale), int(bool(causal)), self._ptr(o),
+                                               self._ptr(lse), threads or self.default_threads())
+        if st != 0:
+            raise OracleError("oracle_attention_decode returned %d" % st)
+        return o, lse
 
     def attention_bwd(self, q, k, v, g, scale, causal=False, threads=None):
         """Gradients (dq, dk, dv) of sum(o * g) for the plain definition.

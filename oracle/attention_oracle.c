@@ -38,6 +38,8 @@
  *    tests can check the page's hand-worked intermediate values
  *    (section 3.6.5) and the block-order independence the page claims.
  *
+ *  - oracle_attention_decode: the plain definition for Nq queries against
+ *    Nk >= Nq keys (decoding; causal aligns the queries with the end).
  *  - oracle_attention_bwd: the gradients of the plain definition (softmax
  *    Jacobian), for the backward pass; oracle_attention_bwd_rows: dq of
  *    listed query rows only (O(N d) each, for full-size samples).
@@ -78,12 +80,12 @@ static long allowed_keys(long i, long n, int causal)
     return n;
 }
 
-/* Plain definition for one row: stable softmax of the scores, times V. */
-static void attention_row(const double *q, const double *k, const double *v,
-                          long i, long n, long d, double scale, int causal,
-                          double *s, double *o_i, double *lse_i)
+/* Plain definition for one query row against its first n_keys keys:
+ * stable softmax of the scores, times V. */
+static void attention_row_keys(const double *q, const double *k, const double *v,
+                               long i, long n_keys, long d, double scale,
+                               double *s, double *o_i, double *lse_i)
 {
-    long n_keys = allowed_keys(i, n, causal);
     scores_row(q, k, i, n_keys, d, scale, s);
 
     double m = -INFINITY;
@@ -106,6 +108,14 @@ static void attention_row(const double *q, const double *k, const double *v,
         o_i[c] = o_i[c] / l;
 
     *lse_i = m + log(l);
+}
+
+/* Plain definition for row i of a square (queries = keys = n) problem. */
+static void attention_row(const double *q, const double *k, const double *v,
+                          long i, long n, long d, double scale, int causal,
+                          double *s, double *o_i, double *lse_i)
+{
+    attention_row_keys(q, k, v, i, allowed_keys(i, n, causal), d, scale, s, o_i, lse_i);
 }
 
 /* ------------------------------------------------------------------ */
@@ -644,6 +654,99 @@ int oracle_attention_bwd_rows(const double *q, const double *k, const double *v,
             spawned[t] = 1;
         else
             dq_rows_worker(jb);
+    }
+    int status = ORACLE_OK;
+    for (int t = 0; t < nthreads; ++t) {
+        if (spawned[t])
+            pthread_join(tids[t], NULL);
+        if (jobs[t].status != ORACLE_OK)
+            status = jobs[t].status;
+    }
+    free(jobs); free(tids); free(spawned);
+    return status;
+}
+
+/* ------------------------------------------------------------------ */
+/* Decoding: few queries against a long key sequence.                   */
+/*
+ * The plain definition for Nq queries against Nk keys (Nq <= Nk).  Causal
+ * aligns the queries with the end of the key sequence: query i sits at
+ * position Nk - Nq + i and attends to keys 0 .. Nk - Nq + i (for Nq = 1,
+ * every key).  "3.6 어텐션 I", section 3.6.9: decoding (one query) is the
+ * case that needs a different parallelisation; the quantity is unchanged.
+ */
+static long decode_keys(long i, long nq, long nk, int causal)
+{
+    return causal ? nk - nq + i + 1 : nk;
+}
+
+typedef struct {
+    const double *q, *k, *v;
+    long nq, nk, d;
+    double scale;
+    int causal;
+    double *o, *lse;
+    long begin, end; /* flattened (head, query) rows */
+    int status;
+} decode_job;
+
+static void *decode_worker(void *arg)
+{
+    decode_job *jb = (decode_job *)arg;
+    double *s = (double *)malloc((size_t)jb->nk * sizeof(double));
+    if (!s) {
+        jb->status = ORACLE_ENOMEM;
+        return NULL;
+    }
+    for (long r = jb->begin; r < jb->end; ++r) {
+        const long bh = r / jb->nq, i = r % jb->nq;
+        attention_row_keys(jb->q + bh * jb->nq * jb->d, jb->k + bh * jb->nk * jb->d,
+                           jb->v + bh * jb->nk * jb->d, i, decode_keys(i, jb->nq, jb->nk, jb->causal),
+                           jb->d, jb->scale, s, jb->o + r * jb->d, jb->lse + r);
+    }
+    free(s);
+    jb->status = ORACLE_OK;
+    return NULL;
+}
+
+/*
+ * oracle_attention_decode: q [BH, Nq, d], k and v [BH, Nk, d] fp64
+ * contiguous; o [BH, Nq, d], lse [BH, Nq].  Requires 1 <= Nq <= Nk.
+ */
+int oracle_attention_decode(const double *q, const double *k, const double *v, long BH, long Nq,
+                            long Nk, long d, double scale, int causal, double *o, double *lse,
+                            int nthreads)
+{
+    if (BH < 0 || Nq < 1 || Nk < Nq || d < 1 || (causal != 0 && causal != 1))
+        return ORACLE_EINVAL;
+    if (BH == 0)
+        return ORACLE_OK;
+    if (!q || !k || !v || !o || !lse)
+        return ORACLE_EINVAL;
+    const long nrows = BH * Nq;
+    if (nthreads <= 0)
+        nthreads = 1;
+    if (nthreads > nrows)
+        nthreads = (int)nrows;
+    decode_job *jobs = (decode_job *)calloc((size_t)nthreads, sizeof(decode_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    unsigned char *spawned = (unsigned char *)calloc((size_t)nthreads, 1);
+    if (!jobs || !tids || !spawned) {
+        free(jobs); free(tids); free(spawned);
+        return ORACLE_ENOMEM;
+    }
+    const long per = (nrows + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        decode_job *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v; jb->nq = Nq; jb->nk = Nk; jb->d = d;
+        jb->scale = scale; jb->causal = causal; jb->o = o; jb->lse = lse;
+        jb->begin = t * per < nrows ? t * per : nrows;
+        jb->end = (t + 1) * per < nrows ? (t + 1) * per : nrows;
+        jb->status = ORACLE_OK;
+        if (t < nthreads - 1 && pthread_create(&tids[t], NULL, decode_worker, jb) == 0)
+            spawned[t] = 1;
+        else
+            decode_worker(jb);
     }
     int status = ORACLE_OK;
     for (int t = 0; t < nthreads; ++t) {

@@ -12,6 +12,7 @@ Sources (page title, section):
     3.6.5  worked example (tests/golden/p4_worked_example.json)
     3.6.6  causal: keys j > i are skipped
     3.6.7  saved statistic L = m + log l; the backward pass recomputes S, P
+    3.6.9  decoding (one query) needs another parallelisation: Nq << Nk
     3.6.10 pitfalls: rescale both l and O; never drop the max shift
     3.6.11 exercise 2 (tests/golden/p4_exercise2.json)
 """
@@ -445,6 +446,54 @@ def pin_bwd_row_split_matches_whole_heads(orc):
                "dq rows vs whole (causal=%d)" % causal)
 
 
+# ---------------------------------------------------------------------------
+# Decoding (section 3.6.9: a few queries against a long key sequence).
+
+def pin_decode_square_is_the_forward(orc):
+    """Nq = Nk: the decode definition is the square one (causal included:
+    with Nq = Nk the end-aligned and start-aligned masks coincide)."""
+    rng = np.random.default_rng(4646)
+    q, k, v = (rng.standard_normal((2, 1, 13, 5)) for _ in range(3))
+    for causal in (False, True):
+        o1, l1 = orc.attention_decode(q, k, v, 0.6, causal=causal, threads=2)
+        o2, l2 = orc.attention_fwd(q, k, v, 0.6, causal=causal, threads=1)
+        _close(o1, o2, 0.0, "decode square O (causal=%d)" % causal)
+        _close(l1, l2, 0.0, "decode square LSE (causal=%d)" % causal)
+
+
+def pin_decode_end_alignment(orc):
+    """Causal decode: the last query sees every key (= non-causal); query i
+    sees exactly the first Nk - Nq + i + 1 keys (= non-causal on that prefix)."""
+    rng = np.random.default_rng(4747)
+    Nq, Nk = 4, 23
+    q = rng.standard_normal((1, 2, Nq, 6))
+    k, v = (rng.standard_normal((1, 2, Nk, 6)) for _ in range(2))
+    oc, lc = orc.attention_decode(q, k, v, 0.5, causal=True)
+    on, ln = orc.attention_decode(q, k, v, 0.5, causal=False)
+    _close(oc[:, :, -1], on[:, :, -1], 0.0, "last query sees all keys")
+    for i in range(Nq):
+        n = Nk - Nq + i + 1
+        oi, li = orc.attention_decode(q[:, :, i:i + 1], k[:, :, :n], v[:, :, :n], 0.5)
+        _close(oc[:, :, i], oi[:, :, 0], 1e-15, "query %d on its key prefix" % i)
+        _close(lc[:, :, i], li[:, :, 0], 1e-15, "query %d LSE on its key prefix" % i)
+
+
+def pin_decode_uniform_and_permutation(orc):
+    """One query, scale 0: O = mean of V and LSE = ln Nk; permuting the keys
+    (with their values) changes nothing (non-causal)."""
+    rng = np.random.default_rng(4848)
+    q = rng.standard_normal((1, 3, 1, 4))
+    k, v = (rng.standard_normal((1, 3, 31, 4)) for _ in range(2))
+    o, l = orc.attention_decode(q, k, v, 0.0)
+    _close(o[:, :, 0], v.mean(axis=2), 1e-14, "scale 0 mean")
+    _close(l, np.full((1, 3, 1), math.log(31)), 1e-14, "scale 0 LSE")
+    perm = rng.permutation(31)
+    o1, l1 = orc.attention_decode(q, k, v, 0.7)
+    o2, l2 = orc.attention_decode(q, k[:, :, perm], v[:, :, perm], 0.7)
+    _close(o2, o1, 1e-14, "key permutation O")
+    _close(l2, l1, 1e-14, "key permutation LSE")
+
+
 PINS = [
     pin_worked_example_full,
     pin_worked_example_online,
@@ -466,4 +515,7 @@ PINS = [
     pin_bwd_value_shift,
     pin_bwd_causal_first_row,
     pin_bwd_row_split_matches_whole_heads,
+    pin_decode_square_is_the_forward,
+    pin_decode_end_alignment,
+    pin_decode_uniform_and_permutation,
 ]

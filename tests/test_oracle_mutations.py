@@ -41,6 +41,9 @@ MUTATIONS = [
     ("bwd_split_sum_first_job_only", "const rows_job *jb = &jobs[h * splits + sp];",
      "const rows_job *jb = &jobs[h * splits];"),
     ("bwd_rows_ignore_causal", "allowed_keys(i, jb->N, jb->causal)", "allowed_keys(i, jb->N, 0)"),
+    ("decode_causal_start_aligned", "return causal ? nk - nq + i + 1 : nk;", "return causal ? i + 1 : nk;"),
+    ("decode_causal_off_by_one", "return causal ? nk - nq + i + 1 : nk;", "return causal ? nk - nq + i : nk;"),
+    ("decode_key_head_stride", "jb->k + bh * jb->nk * jb->d,", "jb->k + bh * jb->nq * jb->d,"),
     ("bwd_dv_uses_ds", "dv[j * d + c] += s[j] * g[i * d + c];", "dv[j * d + c] += ds * g[i * d + c];"),
     ("bwd_ds_not_centred", "double ds = s[j] * (dp[j] - pdp);", "double ds = s[j] * dp[j];"),
     ("bwd_ds_sign", "double ds = s[j] * (dp[j] - pdp);", "double ds = s[j] * (pdp - dp[j]);"),
