@@ -3,17 +3,21 @@
 ``fa_fwd(q, k, v, ...)`` computes O = softmax(Q K^T * scale) V and the row
 log-sum-exp for contiguous [B, H, N, d] fp16/bf16 CUDA tensors by calling the
 C ABI (include/fa.h) of the in-tree CUDA library on the current torch stream;
-``fa_bwd`` computes the gradients of q, k, v from the forward's o and lse.
+``fa_bwd`` computes the gradients of q, k, v from the forward's o and lse;
+``fa_decode`` runs a few query rows per head against a long KV sequence
+(split-KV).
 PyTorch only supplies device memory and the stream; every step of the
 computation runs in the library's kernel.  There is no CPU or eager fallback:
 without the built library, or off a CUDA device, calls raise ``FAError``.
 """
 from ._lib import (FA_BF16, FA_FP16, FAError, fa1_fwd_raw, fa1_fwd_workspace_size,
-                   fa_abi_version, fa_bwd_raw, fa_bwd_workspace_size, fa_fwd_raw,
-                   fa_last_device_status, fa_selftest_wait_timeout, fa_status_str, lib_path, load)
+                   fa_abi_version, fa_bwd_raw, fa_bwd_workspace_size, fa_decode_raw,
+                   fa_decode_workspace_size, fa_fwd_raw, fa_last_device_status,
+                   fa_selftest_wait_timeout, fa_status_str, lib_path, load)
 
 __all__ = ["fa_fwd", "fa_fwd_raw", "fa1_fwd", "fa1_fwd_raw", "fa1_fwd_workspace_size",
            "fa_bwd", "fa_bwd_raw", "fa_bwd_workspace_size",
+           "fa_decode", "fa_decode_raw", "fa_decode_workspace_size",
            "fa_last_device_status", "fa_selftest_wait_timeout",
            "fa_status_str", "fa_abi_version", "FAError", "load", "lib_path"]
 
@@ -164,3 +168,38 @@ def fa_bwd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv
     if st != 0:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv
+
+
+def fa_decode(q, k, v, o=None, lse=None, scale=None, causal=False, return_lse=True, workspace=None,
+              stream=None):
+    """Decoding attention: q [B, H, Nq, d] (1 <= Nq <= 16) against k, v
+    [B, H, Nk, d] (Nk >= Nq), CUDA tensors of one 16-bit dtype.  causal puts
+    the queries at the end of the sequence.  Returns (o, lse)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise FAError(1, "%s must be a CUDA tensor" % name)
+        if t.dim() != 4 or not t.is_contiguous():
+            raise FAError(1, "%s must be a contiguous [B, H, N, d] tensor" % name)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if (k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != d
+            or k.dtype != q.dtype or v.dtype != q.dtype):
+        raise FAError(1, "k, v must be [B, H, Nk, d] like q")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = float(d) ** -0.5
+    o, lse = _outputs(q, o, lse, return_lse)
+    need = fa_decode_workspace_size(B, H, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_decode_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), B, H, Nq, Nk, d,
+                           float(scale), int(bool(causal)), code, stream.cuda_stream)
+    if st != 0:
+        raise FAError(st, "fa_decode")
+    return o, lse

@@ -20,8 +20,8 @@ FA_BF16 = 1
 
 # every symbol include/fa.h declares
 EXPORTS = ("fa_fwd", "fa1_fwd_workspace_size", "fa1_fwd", "fa1_fwd_noalloc", "fa_bwd_workspace_size",
-           "fa_bwd", "fa_last_device_status", "fa_selftest_wait_timeout", "fa_status_str",
-           "fa_abi_version")
+           "fa_bwd", "fa_decode_workspace_size", "fa_decode", "fa_last_device_status",
+           "fa_selftest_wait_timeout", "fa_status_str", "fa_abi_version")
 
 _lib = None
 
@@ -63,6 +63,10 @@ def load(path=None):
     lib.fa_bwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, f, i,
                            i, vp]
+    lib.fa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_decode.restype = i
+    lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, i, i, vp]
     lib.fa_last_device_status.restype = i
     lib.fa_last_device_status.argtypes = [vp]
     lib.fa_selftest_wait_timeout.restype = i
@@ -102,6 +106,16 @@ def fa_bwd_raw(q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes, B, H, N, d, scal
     """Direct call of the backward entry point; returns the status."""
     return load().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes, B, H, N, d, scale, causal,
                          dtype, stream)
+
+
+def fa_decode_workspace_size(B, H, Nq, Nk, d):
+    return load().fa_decode_workspace_size(B, H, Nq, Nk, d)
+
+
+def fa_decode_raw(q, k, v, o, lse, ws, ws_bytes, B, H, Nq, Nk, d, scale, causal, dtype, stream):
+    """Direct call of the decoding entry point; returns the status."""
+    return load().fa_decode(q, k, v, o, lse, ws, ws_bytes, B, H, Nq, Nk, d, scale, causal, dtype,
+                            stream)
 
 
 def fa_last_device_status(stream=None):

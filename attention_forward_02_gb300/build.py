@@ -1,6 +1,6 @@
 """Build the sm_103a CUDA library in-tree (attention_forward_02_gb300/_build/).
 
-Two translation units (forward, backward) compiled in parallel, one
+Three translation units (forward, backward, decoding) compiled in parallel, one
 -gencode (compute_103a -> sm_103a), static cudart, no link against libcuda
 (the TMA encoder is fetched through the runtime's driver entry-point query).
 Compiles in well under a minute.
@@ -17,9 +17,10 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB = os.path.join(OUT_DIR, LIB_NAME)
-SOURCES = [os.path.join(CSRC, "fa_fwd.cu"), os.path.join(CSRC, "fa_bwd.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa1_fwd_kernel.cuh",
-                                                  "fa_bwd_kernel.cuh", "fa_common.cuh",
+                                                  "fa_bwd_kernel.cuh", "fa_decode_kernel.cuh",
+                                                  "fa_common.cuh",
                                                   "fa_host.h", "sm100_ptx.cuh")] + [
     os.path.join(INCLUDE, "fa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,389 @@
+// fa_decode_kernel.cuh -- attention for decoding on sm_103a: a few queries
+// (1 <= Nq <= 16) per head against a long key sequence (Nk keys).
+//
+// What it computes is the attention of the forward kernel, O = softmax(Q K^T
+// scale) V and LSE, for Nq query rows that sit at the end of the sequence
+// (causal: query i attends to keys 0 .. Nk - Nq + i).  "3.6 어텐션 I —
+// 메모리 문제·FlashAttention 원리", section 3.6.9 notes that decoding (one
+// query) needs a different parallelisation: with one query per head there is
+// no Q block to spread over the SMs, and the work is a single pass over K and
+// V (about Nq flop per byte, far below the tensor-core ridge), so the time is
+// the time to stream K and V from HBM.
+//
+// Split-KV: the keys of each head are cut into chunks of whole 128-key tiles;
+//   fa_decode_split_kernel   persistent, one CTA per SM walking (batch*head,
+//                            chunk) items; the producer streams the K/V tiles
+//                            of its items back to back through a TMA ring;
+//                            per item the compute warps run the online
+//                            softmax of section 3.6.4 over them (running max
+//                            m, per-thread partial sums l, unnormalised O),
+//                            leaving (m, l, O) of the chunk in a workspace;
+//   fa_decode_combine_kernel merges the chunks of each query with the same
+//                            algebra (the result does not depend on how the
+//                            keys are cut, section 3.6.4), and writes O / l and
+//                            LSE.
+// The arithmetic is on the CUDA cores (fp32); tensor cores would idle on a
+// 1..16-row product that HBM cannot feed anyway.
+//
+// Warp roles of the split kernel (160 threads): warps 0-3 compute, warp 4 TMA
+// producer.  Per tile and query:
+//   scores   thread r takes key r of the tile: s' = (q scale log2 e) . k_r;
+//   max      warp shuffles, then the four warps' maxima through shared memory;
+//   p        p_r = 2^(s' - m_new), l_r = l_r alpha + p_r (alpha = 2^(m_old - m_new)),
+//            written to shared memory for the next phase;
+//   P V      thread t takes a column pair of V and a group of the tile's keys:
+//            o = o alpha + sum_j p_j v_j (fp32).
+// Every mbarrier wait is bounded, as in the other kernels.
+#pragma once
+
+#include "fa_common.cuh"
+
+namespace fa {
+namespace dec {
+
+constexpr int kTileKeys = 128;
+constexpr int kComputeThreads = 128;
+constexpr int kProducerWarp = 4;
+constexpr int kThreads = 160;
+constexpr int kMaxNq = 16;
+
+template <int D>
+struct Cfg {
+    static constexpr int TILE = kTileKeys * D * 2;   // one [128, D] 16-bit K or V tile
+    static constexpr int STAGES = D == 64 ? 6 : 3;   // 192 KiB of K/V in flight per SM
+    static constexpr int GROUPS = 256 / D;           // key groups of the P V phase
+    static constexpr int KV_OFF = 0;                 // stage s: K at 2 s TILE, V at (2 s + 1) TILE
+    static constexpr int QF_OFF = KV_OFF + STAGES * 2 * TILE;     // fp32 [kMaxNq][D]
+    static constexpr int PS_OFF = QF_OFF + kMaxNq * D * 4;        // fp32 [kMaxNq][kTileKeys]
+    static constexpr int WM_OFF = PS_OFF + kMaxNq * kTileKeys * 4;  // fp32 [kMaxNq][4] warp maxima / sums
+    static constexpr int RO_OFF = WM_OFF + kMaxNq * 4 * 4;           // fp32 [GROUPS][kMaxNq][D] O reduction
+    static constexpr int BAR_OFF = RO_OFF + GROUPS * kMaxNq * D * 4;
+    static constexpr int B_FULL = 0;
+    static constexpr int B_EMPTY = STAGES;
+    static constexpr int NUM_BARS = 2 * STAGES;
+    static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // abort flag
+    static constexpr int SMEM_USED = SLOT_OFF + 16;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+// 128-bit shared load of 8 16-bit values, widened to fp32.
+template <typename T>
+__device__ __forceinline__ void load8(uint32_t addr, float (&f)[8])
+{
+    const uint4 x = ld_shared_v4(addr);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = DTypeTraits<T>::unpack(w[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Workspace of one launch: for every (batch*head, chunk, query) the chunk's
+// running max m (log2 units of the scaled score), sum l and unnormalised O.
+struct Partials {
+    float *o;  // [BH, splits, Nq, D]
+    float *m;  // [BH, splits, Nq]
+    float *l;  // [BH, splits, Nq]
+};
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                           const T *__restrict__ q, Partials part, int Nq, int Nk, int splits,
+                           int tiles_per_split, int num_items, int causal, float scale_log2)
+{
+    using C = Cfg<D>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int PAIRS = D / 2;                          // column pairs
+    constexpr int KEYS_PER_GROUP = kTileKeys / C::GROUPS;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SLOT_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_tiles = (Nk + kTileKeys - 1) / kTileKeys;
+    // item w = (bh, chunk): keys [t0, t1) x 128 of head bh
+    auto item_tiles = [&](int w, int &bh, int &split, int &t0) -> int {
+        bh = w / splits;
+        split = w % splits;
+        t0 = split * tiles_per_split;
+        return max(0, min(num_tiles, t0 + tiles_per_split) - t0);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(C::B_FULL + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), kComputeThreads);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            // ---------------- producer: the tiles of every item, back to back ----------------
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const uint64_t pol = l2_policy_evict_first();  // K and V are read once
+            int L = 0;  // loads into the ring so far
+            bool ok = true;
+            for (int w = blockIdx.x; ok && w < num_items; w += gridDim.x) {
+                int bh, split, t0;
+                const int nt = item_tiles(w, bh, split, t0);
+                for (int i = 0; i < nt; ++i, ++L) {
+                    const int s = L % STAGES;
+                    if (L >= STAGES && !(ok = wait_bounded(bar(C::B_EMPTY + s), ((L / STAGES) - 1) & 1, abort_flag)))
+                        break;
+                    const uint32_t kdst = sbase + C::KV_OFF + (2 * s) * C::TILE;
+                    mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE);
+                    for (int b = 0; b < D / 64; ++b) {
+                        tma_load_3d(kdst + b * kSwAtomBytes, &tm_k, bar(C::B_FULL + s), b * 64,
+                                    (t0 + i) * kTileKeys, bh, pol);
+                        tma_load_3d(kdst + C::TILE + b * kSwAtomBytes, &tm_v, bar(C::B_FULL + s), b * 64,
+                                    (t0 + i) * kTileKeys, bh, pol);
+                    }
+                }
+            }
+            for (int s = 0; s < STAGES; ++s)
+                if (L > s)
+                    drain_bounded(bar(C::B_FULL + s), ((L - 1 - s) / STAGES) & 1);
+        }
+    } else {
+        // ---------------- compute warps ----------------
+        const int r = threadIdx.x;              // key of the tile (score phase)
+        const int pair = r % PAIRS;             // column pair (P V phase)
+        const int grp = r / PAIRS;              // key group (P V phase)
+        int L = 0;                              // tiles consumed so far (all items)
+        bool ok = true;
+        for (int w = blockIdx.x; ok && w < num_items; w += gridDim.x) {
+            int bh, split, t0;
+            const int nt = item_tiles(w, bh, split, t0);
+            // q of this head, pre-multiplied by scale * log2(e), as fp32 (the
+            // previous item's last barrier below has retired every read of it)
+            for (int x = r; x < Nq * D; x += kComputeThreads) {
+                const uint16_t bits = reinterpret_cast<const uint16_t *>(q)[static_cast<size_t>(bh) * Nq * D + x];
+                st_shared_f32(sbase + C::QF_OFF + 4u * x,
+                              DTypeTraits<T>::unpack(static_cast<uint32_t>(bits)).x * scale_log2);
+            }
+            named_bar_sync(1, kComputeThreads);
+            float m[kMaxNq], l[kMaxNq];
+            float2 o[kMaxNq];
+#pragma unroll
+            for (int qi = 0; qi < kMaxNq; ++qi) {
+                m[qi] = -INFINITY;
+                l[qi] = 0.f;
+                o[qi] = make_float2(0.f, 0.f);
+            }
+            for (int i = 0; i < nt; ++i, ++L) {
+                const int s = L % STAGES;
+                ok = wait_bounded(bar(C::B_FULL + s), (L / STAGES) & 1, abort_flag);
+                // one decision for all four warps: the named barriers below need them all
+                if (named_bar_or(3, kComputeThreads, !ok || *abort_flag != 0)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t ktile = sbase + C::KV_OFF + (2 * s) * C::TILE;
+                const uint32_t vtile = ktile + C::TILE;
+                const int key = (t0 + i) * kTileKeys + r;
+                // ---- scores of key r against every query ----
+                float acc[kMaxNq];
+#pragma unroll
+                for (int qi = 0; qi < kMaxNq; ++qi)
+                    acc[qi] = 0.f;
+#pragma unroll 2
+                for (int c8 = 0; c8 < D / 8; ++c8) {
+                    float kf[8];
+                    load8<T>(ktile + sw128_offset(r, c8), kf);
+#pragma unroll
+                    for (int qi = 0; qi < kMaxNq; ++qi) {
+                        if (qi < Nq) {
+                            const uint8_t *qa = smem + C::QF_OFF + 4 * (qi * D + 8 * c8);
+                            const float4 a = *reinterpret_cast<const float4 *>(qa);
+                            const float4 b = *reinterpret_cast<const float4 *>(qa + 16);
+                            acc[qi] = fmaf(a.x, kf[0], acc[qi]);
+                            acc[qi] = fmaf(a.y, kf[1], acc[qi]);
+                            acc[qi] = fmaf(a.z, kf[2], acc[qi]);
+                            acc[qi] = fmaf(a.w, kf[3], acc[qi]);
+                            acc[qi] = fmaf(b.x, kf[4], acc[qi]);
+                            acc[qi] = fmaf(b.y, kf[5], acc[qi]);
+                            acc[qi] = fmaf(b.z, kf[6], acc[qi]);
+                            acc[qi] = fmaf(b.w, kf[7], acc[qi]);
+                        }
+                    }
+                }
+                // ---- masks, tile maxima ----
+#pragma unroll
+                for (int qi = 0; qi < kMaxNq; ++qi) {
+                    if (qi < Nq) {
+                        const int last = causal ? Nk - Nq + qi : Nk - 1;  // last key query qi may see
+                        if (key > last)
+                            acc[qi] = -INFINITY;
+                        float wm = acc[qi];
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+                        if (lane == 0)
+                            st_shared_f32(sbase + C::WM_OFF + 4u * (qi * 4 + warp), wm);
+                    }
+                }
+                named_bar_sync(1, kComputeThreads);
+                float alpha[kMaxNq];
+#pragma unroll
+                for (int qi = 0; qi < kMaxNq; ++qi) {
+                    alpha[qi] = 1.f;
+                    if (qi < Nq) {
+                        const uint32_t wa = sbase + C::WM_OFF + 4u * (qi * 4);
+                        const float tmax = fmaxf(fmaxf(ld_shared_f32(wa), ld_shared_f32(wa + 4)),
+                                                 fmaxf(ld_shared_f32(wa + 8), ld_shared_f32(wa + 12)));
+                        const float m_new = fmaxf(m[qi], tmax);
+                        float p = 0.f;
+                        if (m_new != -INFINITY) {  // some key of this query seen so far
+                            alpha[qi] = ex2_approx(m[qi] - m_new);
+                            p = ex2_approx(acc[qi] - m_new);
+                            m[qi] = m_new;
+                        }
+                        l[qi] = l[qi] * alpha[qi] + p;
+                        st_shared_f32(sbase + C::PS_OFF + 4u * (qi * kTileKeys + r), p);
+                    }
+                }
+                named_bar_sync(1, kComputeThreads);
+                // ---- P V: column pair `pair`, keys [grp KEYS_PER_GROUP, +KEYS_PER_GROUP) ----
+                const int c8 = (2 * pair) >> 3;
+                const uint32_t in_chunk = static_cast<uint32_t>((2 * pair) & 7) * 2u;
+#pragma unroll
+                for (int qi = 0; qi < kMaxNq; ++qi)
+                    if (qi < Nq)
+                        o[qi] = make_float2(o[qi].x * alpha[qi], o[qi].y * alpha[qi]);
+#pragma unroll 4
+                for (int jj = 0; jj < KEYS_PER_GROUP; ++jj) {
+                    const int j = grp * KEYS_PER_GROUP + jj;
+                    const float2 vv = DTypeTraits<T>::unpack(ld_shared_u32(vtile + sw128_offset(j, c8) + in_chunk));
+#pragma unroll
+                    for (int qi = 0; qi < kMaxNq; ++qi) {
+                        if (qi < Nq) {
+                            const float p = ld_shared_f32(sbase + C::PS_OFF + 4u * (qi * kTileKeys + j));
+                            o[qi] = make_float2(fmaf(p, vv.x, o[qi].x), fmaf(p, vv.y, o[qi].y));
+                        }
+                    }
+                }
+                // the stage (K and V) is free again; the p buffer and the warp
+                // maxima are free once every thread has passed this barrier
+                mbar_arrive(bar(C::B_EMPTY + s));
+                named_bar_sync(1, kComputeThreads);
+            }
+            if (!ok)
+                break;
+            // ---------------- the item's (m, l, O) ----------------
+            // l: sum over the 128 threads (keys); O: sum over the key groups
+#pragma unroll
+            for (int qi = 0; qi < kMaxNq; ++qi) {
+                if (qi < Nq) {
+                    float ws = l[qi];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        ws += __shfl_xor_sync(0xffffffffu, ws, off);
+                    if (lane == 0)
+                        st_shared_f32(sbase + C::WM_OFF + 4u * (qi * 4 + warp), ws);
+                    const uint32_t oa = sbase + C::RO_OFF + 4u * ((grp * kMaxNq + qi) * D + 2 * pair);
+                    st_shared_f32(oa, o[qi].x);
+                    st_shared_f32(oa + 4, o[qi].y);
+                }
+            }
+            named_bar_sync(1, kComputeThreads);
+            const size_t base = (static_cast<size_t>(bh) * splits + split) * Nq;
+            for (int x = r; x < Nq * D; x += kComputeThreads) {
+                const int qi = x / D, c = x % D;
+                float sum = 0.f;
+                for (int g = 0; g < C::GROUPS; ++g)
+                    sum += ld_shared_f32(sbase + C::RO_OFF + 4u * ((g * kMaxNq + qi) * D + c));
+                part.o[(base + qi) * D + c] = sum;
+            }
+            if (r < Nq) {
+                const uint32_t wa = sbase + C::WM_OFF + 4u * (r * 4);
+                part.l[base + r] = ld_shared_f32(wa) + ld_shared_f32(wa + 4) + ld_shared_f32(wa + 8) +
+                                   ld_shared_f32(wa + 12);
+#pragma unroll
+                for (int qi = 0; qi < kMaxNq; ++qi)
+                    if (qi == r)
+                        part.m[base + r] = m[qi];
+            }
+            // every read of the reduction areas and of q is done before the next item
+            named_bar_sync(1, kComputeThreads);
+        }
+    }
+    __syncthreads();
+}
+
+// Merges the chunks of every (batch*head, query): M = max_s m_s,
+// L = sum_s l_s 2^(m_s - M), O = sum_s O_s 2^(m_s - M) / L, LSE = (M + log2 L) ln 2.
+// One warp per (batch*head, query).
+template <int D, typename T>
+__global__ void __launch_bounds__(256) fa_decode_combine_kernel(Partials part, T *__restrict__ out,
+                                                                float *__restrict__ lse, long long rows, int Nq,
+                                                                int splits)
+{
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows)
+        return;
+    const long long bh = row / Nq;
+    const int qi = static_cast<int>(row % Nq);
+    float M = -INFINITY;
+    for (int s = 0; s < splits; ++s)
+        M = fmaxf(M, part.m[(bh * splits + s) * Nq + qi]);
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int c = 0; c < PER; ++c)
+        acc[c] = 0.f;
+    float L = 0.f;
+    for (int s = 0; s < splits; ++s) {
+        const size_t idx = (static_cast<size_t>(bh) * splits + s) * Nq + qi;
+        const float ms = part.m[idx];
+        if (ms == -INFINITY)
+            continue;  // a chunk with no key this query may see
+        const float w = ex2_approx(ms - M);
+        L = fmaf(part.l[idx], w, L);
+#pragma unroll
+        for (int c = 0; c < PER; ++c)
+            acc[c] = fmaf(part.o[idx * D + lane * PER + c], w, acc[c]);
+    }
+    const float inv = 1.f / L;
+    T *dst = out + static_cast<size_t>(row) * D + lane * PER;
+#pragma unroll
+    for (int c = 0; c < PER; c += 2) {
+        const uint32_t w = DTypeTraits<T>::pack(acc[c] * inv, acc[c + 1] * inv);
+        *reinterpret_cast<uint32_t *>(dst + c) = w;
+    }
+    if (lse != nullptr && lane == 0)
+        lse[row] = (M + __log2f(L)) * 0.6931471805599453f;
+}
+
+}  // namespace dec
+}  // namespace fa

@@ -390,10 +390,10 @@ fa_status_t fa_last_device_status(void *stream)
         return FA_ERR_CUDA;
     if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess)
         return FA_ERR_CUDA;
-    unsigned int bwd_word = 0;
-    if (fa_host::take_bwd_status(&bwd_word) != FA_OK)
+    unsigned int bwd_word = 0, dec_word = 0;
+    if (fa_host::take_bwd_status(&bwd_word) != FA_OK || fa_host::take_decode_status(&dec_word) != FA_OK)
         return FA_ERR_CUDA;
-    word |= bwd_word;
+    word |= bwd_word | dec_word;
     if (word & ~fa::kStatusTimeout)
         return FA_ERR_CUDA;  // a self-test wait did not behave as required
     return (word & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;

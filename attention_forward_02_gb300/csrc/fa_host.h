@@ -1,5 +1,6 @@
 // fa_host.h -- host-side helpers shared by the library's translation units
-// (forward entry points in fa_fwd.cu, backward in fa_bwd.cu).  Internal: not
+// (forward entry points in fa_fwd.cu, backward in fa_bwd.cu, decoding in
+// fa_decode.cu).  Internal: not
 // part of the C ABI (the library is built with hidden visibility).
 #pragma once
 
@@ -37,8 +38,9 @@ fa_status_t check_args(const void *q, const void *k, const void *v, const void *
                        int B, int H, int N, int d, float scale, int causal, fa_dtype_t dtype,
                        bool *empty);
 
-// Reads and clears the backward unit's device status word (bit 0: a bounded
-// wait expired); 0 when nothing was recorded.
+// Read and clear the backward / decoding units' device status words (bit 0:
+// a bounded wait expired); 0 when nothing was recorded.
 fa_status_t take_bwd_status(unsigned int *word);
+fa_status_t take_decode_status(unsigned int *word);
 
 }  // namespace fa_host

@@ -11,7 +11,8 @@ two, so the product is exact in fp16/bf16), which spreads the scaled scores to
 a standard deviation of about 8 so that the running max keeps moving.
 
 The backward pass's upstream gradient dO follows the same recipe with a
-seed of its own (``make_dout``).
+seed of its own (``make_dout``); so do the decoding inputs (``make_decode``:
+Nq query rows against an Nk-row KV sequence).
 
 Shapes follow the pages' [B, H, N, d] notation (contiguous, row stride d):
 "Triton으로 FlashAttention 1·2 forward 구현하기", section "기준 shape", uses
@@ -67,6 +68,31 @@ def make_dout(B, H, N, d, dtype="fp16", seed=3):
     dt = torch_dtype(dtype) if isinstance(dtype, str) else dtype
     g = torch.Generator(device="cpu").manual_seed(int(seed))
     return torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(dt).contiguous()
+
+
+# decoding workloads: name -> (B, H, Nq, Nk, d, dtype, (seed_q, seed_k, seed_v), causal)
+DECODE_WORKLOADS = {
+    "decode": (8, 32, 1, 16384, 128, "fp16", (60, 61, 62), False),
+    "decode_spec": (8, 32, 4, 16384, 128, "bf16", (63, 64, 65), True),
+}
+
+
+def make_decode(B, H, Nq, Nk, d, dtype="fp16", seeds=(0, 1, 2)):
+    """q [B, H, Nq, d] and k, v [B, H, Nk, d] (CPU, 16-bit), same recipe as make_qkv."""
+    dt = torch_dtype(dtype) if isinstance(dtype, str) else dtype
+    shapes = ((B, H, Nq, d), (B, H, Nk, d), (B, H, Nk, d))
+    out = []
+    for shape, seed in zip(shapes, seeds):
+        g = torch.Generator(device="cpu").manual_seed(int(seed))
+        out.append(torch.randn(shape, generator=g, dtype=torch.float32).to(dt).contiguous())
+    return tuple(out)
+
+
+def make_decode_workload(name):
+    """(q, k, v, meta) of a named decoding workload."""
+    B, H, Nq, Nk, d, dtype, seeds, causal = DECODE_WORKLOADS[name]
+    q, k, v = make_decode(B, H, Nq, Nk, d, dtype, seeds)
+    return q, k, v, dict(B=B, H=H, Nq=Nq, Nk=Nk, d=d, dtype=dtype, causal=causal)
 
 
 def make_workload(name, q_scale=1.0):

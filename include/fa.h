@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 2
+#define FA_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define FA_API __attribute__((visibility("default")))
@@ -192,6 +192,41 @@ FA_API fa_status_t fa_bwd(const void *q, const void *k, const void *v, const voi
                           const float *lse, const void *dout, void *dq, void *dk, void *dv,
                           void *workspace, size_t workspace_bytes, int B, int H, int N, int d,
                           float scale, int causal, fa_dtype_t dtype, void *stream);
+
+/*
+ * fa_decode_workspace_size -- bytes of device workspace fa_decode needs: at
+ * most one key chunk per 128 keys, each with an fp32 (m, l, O[d]) per query:
+ * B*H*ceil(Nk/128)*Nq*(d+2)*4.  0 for invalid sizes.
+ */
+FA_API size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d);
+
+/*
+ * fa_decode -- attention for decoding (asynchronous): Nq query rows per head
+ * (1 <= Nq <= 16) against Nk >= Nq keys,
+ *     O = softmax(Q K^T * scale) V,   LSE = log(sum_j exp(scale * q_i . k_j)),
+ * with causal = 1 placing the queries at the end of the sequence (query i
+ * attends to keys 0 .. Nk - Nq + i; with Nq = 1 that is every key).  "3.6
+ * 어텐션 I — 메모리 문제·FlashAttention 원리", section 3.6.9: decoding needs a
+ * different parallelisation than the Q-block grid of fa_fwd.  Split-KV: each
+ * head's keys are cut into chunks that run the online softmax of section
+ * 3.6.4 in parallel; a second launch merges the chunks' (m, l, O) with the
+ * same rescaling (the result does not depend on the cut).
+ *
+ *  q       : device, contiguous [B, H, Nq, d] of `dtype`, 16-byte aligned.
+ *  k, v    : device, contiguous [B, H, Nk, d] of `dtype` (a KV cache),
+ *            16-byte aligned.
+ *  o       : device, contiguous [B, H, Nq, d] of `dtype`, 16-byte aligned.
+ *  lse     : [B, H, Nq] fp32 (natural log, as fa_fwd), or NULL.
+ *  workspace : device, 16-byte aligned, >= fa_decode_workspace_size bytes,
+ *            not overlapping any other buffer; contents do not matter.  Calls
+ *            that share a workspace must not run concurrently.
+ *  B, H, d, scale, dtype, stream : as for fa_fwd.
+ * Errors: as fa_fwd, plus FA_ERR_UNSUPPORTED for Nq outside 1..16 and
+ * FA_ERR_INVALID_ARG for Nk < Nq or a missing, short or overlapping workspace.
+ */
+FA_API fa_status_t fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+                             void *workspace, size_t workspace_bytes, int B, int H, int Nq, int Nk,
+                             int d, float scale, int causal, fa_dtype_t dtype, void *stream);
 
 /*
  * fa_last_device_status -- synchronise `stream`, read and clear the device

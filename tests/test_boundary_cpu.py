@@ -134,6 +134,34 @@ def test_bwd_argument_checks(lib, kwargs, status):
     assert call_bwd(**kwargs) == status
 
 
+def test_decode_workspace_size(lib):
+    # one chunk per 128 keys at most, (m, l, O[d]) fp32 per query
+    assert fa.fa_decode_workspace_size(8, 32, 1, 16384, 128) == 256 * 128 * 1 * 130 * 4
+    assert fa.fa_decode_workspace_size(1, 1, 4, 129, 64) == 2 * 4 * 66 * 4
+    assert fa.fa_decode_workspace_size(1, 1, 17, 1000, 64) == 0   # Nq > 16
+    assert fa.fa_decode_workspace_size(1, 1, 4, 3, 64) == 0       # Nk < Nq
+    assert fa.fa_decode_workspace_size(1, 1, 1, 10, 96) == 0
+
+
+def call_decode(ws=W, ws_bytes=1 << 30, **kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=2, Nq=1, Nk=256, d=64, scale=0.125, causal=0, dtype=0)
+    a.update(kw)
+    return fa.fa_decode_raw(a["q"], a["k"], a["v"], a["o"], a["lse"], ws, ws_bytes, a["B"], a["H"],
+                            a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(Nq=17), 2), (dict(Nq=0), 2), (dict(Nk=0), 1), (dict(Nq=4, Nk=3), 1),
+    (dict(d=96), 2), (dict(dtype=3), 2), (dict(causal=5), 1), (dict(scale=float("nan")), 1),
+    (dict(q=0), 1), (dict(ws=0), 1), (dict(ws_bytes=10), 1),
+    (dict(k=K + 8), 3), (dict(lse=L + 1), 3), (dict(ws=W + 4), 3),
+    (dict(o=K), 1), (dict(ws=V), 1),
+    (dict(B=0), 0), (dict(H=0), 0),
+], ids=lambda x: str(x))
+def test_decode_argument_checks(lib, kwargs, status):
+    assert call_decode(**kwargs) == status
+
+
 def test_selftest_rejects_bad_limit_before_cuda(lib):
     assert fa.fa_selftest_wait_timeout(0) == 1
     assert fa.fa_selftest_wait_timeout(2_000_000) == 1

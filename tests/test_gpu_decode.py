@@ -1,0 +1,61 @@
+"""Decoding attention (fa_decode, split-KV) against the fp64 oracle through
+the C ABI, with the forward pass's tolerance (P stays fp32 here, so only the
+output rounding and fp32 sums enter); full checks at the bench sizes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_forward_02_gb300 import inputs
+from parity_util import compare, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return oracle.get()
+
+
+def run_decode(q, k, v, scale, causal):
+    import attention_forward_02_gb300 as fa
+    dev = torch.device("cuda:0")
+    o, lse = fa.fa_decode(q.to(dev), k.to(dev), v.to(dev), scale=scale, causal=causal)
+    st = fa.fa_last_device_status(torch.cuda.current_stream(dev).cuda_stream)
+    assert st == 0, "device status %s" % fa.fa_status_str(st)
+    return o.cpu(), lse.cpu()
+
+
+def check(orc, q, k, v, scale, causal, what):
+    o, lse = run_decode(q, k, v, scale, causal)
+    qf, kf, vf = to_f64(q), to_f64(k), to_f64(v)
+    o_ref, lse_ref = orc.attention_decode(qf, kf, vf, scale, causal=causal)
+    a_ref = None
+    if v.dtype == torch.bfloat16:
+        a_ref, _ = orc.attention_decode(qf, kf, np.abs(vf), scale, causal=causal)
+    return compare(to_f64(o), to_f64(lse), o_ref, lse_ref, float(v.abs().max()), what, v.dtype, a_ref)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (1, 100), (1, 128), (1, 129), (3, 3), (3, 1000),
+                                   (16, 16), (16, 4100), (5, 2048)])
+def test_small(orc, dtype, d, causal, Nq, Nk):
+    q, k, v = inputs.make_decode(2, 3, Nq, Nk, d, dtype, (9000 + Nk, 9100 + Nq, 9200 + d))
+    check(orc, q, k, v, d ** -0.5, causal, "decode Nq%d Nk%d d%d %s causal=%s" % (Nq, Nk, d, dtype, causal))
+
+
+def test_peaked_scores(orc):
+    # q x 8: scaled scores with a standard deviation about 8 (the running max moves)
+    q, k, v = inputs.make_decode(1, 4, 2, 5000, 128, "fp16", (9301, 9302, 9303))
+    check(orc, q * 8, k, v, 128 ** -0.5, True, "decode peaked")
+
+
+@pytest.mark.parametrize("name", sorted(inputs.DECODE_WORKLOADS))
+def test_workload_full(orc, name):
+    """The bench's decoding workloads, every output row checked."""
+    q, k, v, meta = inputs.make_decode_workload(name)
+    check(orc, q, k, v, meta["d"] ** -0.5, meta["causal"], "decode workload %s" % name)
