@@ -25,20 +25,31 @@ struct DecState {
 };
 DecState g_dec[kMaxDevices];
 
-template <int D, typename T>
+template <int D, int NQ, typename T>
 cudaError_t set_smem_attr()
 {
-    return cudaFuncSetAttribute(fa::dec::fa_decode_split_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                fa::dec::Cfg<D>::SMEM_ALLOC);
+    return cudaFuncSetAttribute(fa::dec::fa_decode_split_kernel<D, NQ, T>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, fa::dec::Cfg<D, NQ>::SMEM_ALLOC);
+}
+
+template <int D, typename T>
+cudaError_t set_smem_attr_all()
+{
+    cudaError_t e = set_smem_attr<D, 1, T>();
+    if (e == cudaSuccess) e = set_smem_attr<D, 2, T>();
+    if (e == cudaSuccess) e = set_smem_attr<D, 4, T>();
+    if (e == cudaSuccess) e = set_smem_attr<D, 8, T>();
+    if (e == cudaSuccess) e = set_smem_attr<D, 16, T>();
+    return e;
 }
 
 void init_dec(DecState &st)
 {
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem_attr<64, __half>();
-    if (e == cudaSuccess) e = set_smem_attr<128, __half>();
-    if (e == cudaSuccess) e = set_smem_attr<64, __nv_bfloat16>();
-    if (e == cudaSuccess) e = set_smem_attr<128, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_all<64, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_all<128, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_all<64, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_all<128, __nv_bfloat16>();
     st.err = e;
 }
 
@@ -59,9 +70,9 @@ void plan(long long BH, int Nk, int num_sms, int *splits, int *tiles_per_split)
     *splits = static_cast<int>((tiles + per - 1) / per);
 }
 
-template <int D, typename T>
-fa_status_t launch(const CUtensorMap &mk, const CUtensorMap &mv, const void *q, void *o, float *lse, float *ws,
-                   int BH, int Nq, int Nk, float scale, int causal, int num_sms, cudaStream_t stream)
+template <int D, int NQ, typename T>
+fa_status_t launch_nq(const CUtensorMap &mk, const CUtensorMap &mv, const void *q, void *o, float *lse, float *ws,
+                      int BH, int Nq, int Nk, float scale, int causal, int num_sms, cudaStream_t stream)
 {
     using namespace fa::dec;
     int splits = 1, per = 1;
@@ -73,12 +84,28 @@ fa_status_t launch(const CUtensorMap &mk, const CUtensorMap &mv, const void *q, 
     const int items = BH * splits;
     const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    fa_decode_split_kernel<D, T><<<grid, kThreads, Cfg<D>::SMEM_ALLOC, stream>>>(
+    fa_decode_split_kernel<D, NQ, T><<<grid, kThreads, Cfg<D, NQ>::SMEM_ALLOC, stream>>>(
         mk, mv, static_cast<const T *>(q), part, Nq, Nk, splits, per, items, causal, scale_log2);
     const long long rows = static_cast<long long>(BH) * Nq;
     fa_decode_combine_kernel<D, T><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
         part, static_cast<T *>(o), lse, rows, Nq, splits);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// The query count rounds up to the next compiled one (1, 2, 4, 8, 16).
+template <int D, typename T>
+fa_status_t launch(const CUtensorMap &mk, const CUtensorMap &mv, const void *q, void *o, float *lse, float *ws,
+                   int BH, int Nq, int Nk, float scale, int causal, int num_sms, cudaStream_t stream)
+{
+    if (Nq <= 1)
+        return launch_nq<D, 1, T>(mk, mv, q, o, lse, ws, BH, Nq, Nk, scale, causal, num_sms, stream);
+    if (Nq <= 2)
+        return launch_nq<D, 2, T>(mk, mv, q, o, lse, ws, BH, Nq, Nk, scale, causal, num_sms, stream);
+    if (Nq <= 4)
+        return launch_nq<D, 4, T>(mk, mv, q, o, lse, ws, BH, Nq, Nk, scale, causal, num_sms, stream);
+    if (Nq <= 8)
+        return launch_nq<D, 8, T>(mk, mv, q, o, lse, ws, BH, Nq, Nk, scale, causal, num_sms, stream);
+    return launch_nq<D, 16, T>(mk, mv, q, o, lse, ws, BH, Nq, Nk, scale, causal, num_sms, stream);
 }
 
 }  // namespace

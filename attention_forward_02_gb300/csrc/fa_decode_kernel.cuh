@@ -25,14 +25,19 @@
 // The arithmetic is on the CUDA cores (fp32); tensor cores would idle on a
 // 1..16-row product that HBM cannot feed anyway.
 //
-// Warp roles of the split kernel (160 threads): warps 0-3 compute, warp 4 TMA
+// Warp roles of the split kernel (288 threads): warps 0-7 compute, warp 8 TMA
 // producer.  Per tile and query:
-//   scores   thread r takes key r of the tile: s' = (q scale log2 e) . k_r;
-//   max      warp shuffles, then the four warps' maxima through shared memory;
+//   scores   threads 2r, 2r + 1 take key r of the tile, half of d each:
+//            s' = (q scale log2 e) . k_r in packed fp32 FMAs, halves summed by
+//            a lane shuffle;
+//   max      warp shuffles, then the eight warps' maxima through shared memory;
 //   p        p_r = 2^(s' - m_new), l_r = l_r alpha + p_r (alpha = 2^(m_old - m_new)),
 //            written to shared memory for the next phase;
 //   P V      thread t takes a column pair of V and a group of the tile's keys:
-//            o = o alpha + sum_j p_j v_j (fp32).
+//            o = o alpha + sum_j p_j v_j (fp32), a fully unrolled loop whose
+//            swizzled shared-memory offsets are compile-time constants.
+// The number of queries is a template parameter NQ in {1, 2, 4, 8, 16} (the
+// launch rounds Nq up; rows past Nq are computed on zero queries and dropped).
 // Every mbarrier wait is bounded, as in the other kernels.
 #pragma once
 
@@ -42,28 +47,38 @@ namespace fa {
 namespace dec {
 
 constexpr int kTileKeys = 128;
-constexpr int kComputeThreads = 128;
-constexpr int kProducerWarp = 4;
-constexpr int kThreads = 160;
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kProducerWarp = kComputeWarps;
+constexpr int kThreads = kComputeThreads + 32;
 constexpr int kMaxNq = 16;
 
-template <int D>
+template <int D, int NQ>
 struct Cfg {
     static constexpr int TILE = kTileKeys * D * 2;   // one [128, D] 16-bit K or V tile
-    static constexpr int STAGES = D == 64 ? 6 : 3;   // 192 KiB of K/V in flight per SM
-    static constexpr int GROUPS = 256 / D;           // key groups of the P V phase
+    static constexpr int PAIRS = D / 2;              // column pairs of the P V phase
+    static constexpr int GROUPS = kComputeThreads / PAIRS;  // key groups of the P V phase
+    static constexpr int KEYS_PER_GROUP = kTileKeys / GROUPS;
+    // per-CTA areas besides the ring (q, p, warp maxima, O reduction, barriers, slack)
+    static constexpr int EXTRA = NQ * D * 4 + NQ * kTileKeys * 4 + NQ * kComputeWarps * 4 +
+                                 GROUPS * NQ * D * 4 + 8 * 2 * 6 + 16 + 1024;
+    // up to 192 KiB of K/V in flight per SM, as far as the budget allows
+    static constexpr int MAX_STAGES = (227 * 1024 - EXTRA) / (2 * TILE);
+    static constexpr int STAGES = (D == 64 ? 6 : 3) < MAX_STAGES ? (D == 64 ? 6 : 3) : MAX_STAGES;
+    static_assert(STAGES >= 2, "at least a double-buffered ring");
     static constexpr int KV_OFF = 0;                 // stage s: K at 2 s TILE, V at (2 s + 1) TILE
-    static constexpr int QF_OFF = KV_OFF + STAGES * 2 * TILE;     // fp32 [kMaxNq][D]
-    static constexpr int PS_OFF = QF_OFF + kMaxNq * D * 4;        // fp32 [kMaxNq][kTileKeys]
-    static constexpr int WM_OFF = PS_OFF + kMaxNq * kTileKeys * 4;  // fp32 [kMaxNq][4] warp maxima / sums
-    static constexpr int RO_OFF = WM_OFF + kMaxNq * 4 * 4;           // fp32 [GROUPS][kMaxNq][D] O reduction
-    static constexpr int BAR_OFF = RO_OFF + GROUPS * kMaxNq * D * 4;
+    static constexpr int QF_OFF = KV_OFF + STAGES * 2 * TILE;     // fp32 [NQ][D]
+    static constexpr int PS_OFF = QF_OFF + NQ * D * 4;            // fp32 [NQ][kTileKeys]
+    static constexpr int WM_OFF = PS_OFF + NQ * kTileKeys * 4;    // fp32 [NQ][kComputeWarps]
+    static constexpr int RO_OFF = WM_OFF + NQ * kComputeWarps * 4;  // fp32 [GROUPS][NQ][D] O reduction
+    static constexpr int BAR_OFF = RO_OFF + GROUPS * NQ * D * 4;
     static constexpr int B_FULL = 0;
     static constexpr int B_EMPTY = STAGES;
     static constexpr int NUM_BARS = 2 * STAGES;
     static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // abort flag
     static constexpr int SMEM_USED = SLOT_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
+    static_assert(KEYS_PER_GROUP % 8 == 0, "key groups start on a swizzle period");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -106,16 +121,15 @@ struct Partials {
     float *l;  // [BH, splits, Nq]
 };
 
-template <int D, typename T>
+template <int D, int NQ, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const T *__restrict__ q, Partials part, int Nq, int Nk, int splits,
                            int tiles_per_split, int num_items, int causal, float scale_log2)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, NQ>;
     constexpr int STAGES = C::STAGES;
-    constexpr int PAIRS = D / 2;                          // column pairs
-    constexpr int KEYS_PER_GROUP = kTileKeys / C::GROUPS;
+    constexpr int HALF_CHUNKS = D / 16;  // 16-byte chunks in half a key row
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -127,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int num_tiles = (Nk + kTileKeys - 1) / kTileKeys;
-    // item w = (bh, chunk): keys [t0, t1) x 128 of head bh
+    // item w = (bh, chunk): key tiles [t0, t0 + count) of head bh
     auto item_tiles = [&](int w, int &bh, int &split, int &t0) -> int {
         bh = w / splits;
         split = w % splits;
@@ -176,26 +190,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- compute warps ----------------
-        const int r = threadIdx.x;              // key of the tile (score phase)
-        const int pair = r % PAIRS;             // column pair (P V phase)
-        const int grp = r / PAIRS;              // key group (P V phase)
-        int L = 0;                              // tiles consumed so far (all items)
+        const int t = threadIdx.x;
+        const int key_r = t >> 1;           // score phase: key of the tile ...
+        const int half = t & 1;             // ... and which half of d
+        const int pair = t % C::PAIRS;      // P V phase: column pair ...
+        const int grp = t / C::PAIRS;       // ... and key group
+        // score phase: byte offset of 16-byte chunk c of this thread's half row
+        // (16-byte chunks XOR-swizzled by row % 8 inside 128-byte rows; the two
+        // 64-column blocks of D = 128 are kSwAtomBytes apart)
+        const uint32_t krow = static_cast<uint32_t>(key_r) * 128u;
+        // P V phase: the column pair's 16-byte chunk and its offset inside it
+        const int pc8 = (2 * pair) >> 3;
+        const uint32_t pv_col = static_cast<uint32_t>((pc8 >> 3) * kSwAtomBytes) + (static_cast<uint32_t>((2 * pair) & 7) * 2u);
+        int L = 0;  // tiles consumed so far (all items)
         bool ok = true;
         for (int w = blockIdx.x; ok && w < num_items; w += gridDim.x) {
             int bh, split, t0;
             const int nt = item_tiles(w, bh, split, t0);
-            // q of this head, pre-multiplied by scale * log2(e), as fp32 (the
-            // previous item's last barrier below has retired every read of it)
-            for (int x = r; x < Nq * D; x += kComputeThreads) {
-                const uint16_t bits = reinterpret_cast<const uint16_t *>(q)[static_cast<size_t>(bh) * Nq * D + x];
-                st_shared_f32(sbase + C::QF_OFF + 4u * x,
-                              DTypeTraits<T>::unpack(static_cast<uint32_t>(bits)).x * scale_log2);
+            // q of this head, pre-multiplied by scale * log2(e), as fp32; rows
+            // past Nq are zero (the previous item's last barrier has retired
+            // every read of this area)
+            for (int x = t; x < NQ * D; x += kComputeThreads) {
+                float val = 0.f;
+                if (x < Nq * D) {
+                    const uint16_t bits = reinterpret_cast<const uint16_t *>(q)[static_cast<size_t>(bh) * Nq * D + x];
+                    val = DTypeTraits<T>::unpack(static_cast<uint32_t>(bits)).x * scale_log2;
+                }
+                st_shared_f32(sbase + C::QF_OFF + 4u * x, val);
             }
             named_bar_sync(1, kComputeThreads);
-            float m[kMaxNq], l[kMaxNq];
-            float2 o[kMaxNq];
+            float m[NQ], l[NQ];
+            float2 o[NQ];
 #pragma unroll
-            for (int qi = 0; qi < kMaxNq; ++qi) {
+            for (int qi = 0; qi < NQ; ++qi) {
                 m[qi] = -INFINITY;
                 l[qi] = 0.f;
                 o[qi] = make_float2(0.f, 0.f);
@@ -203,92 +230,97 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < nt; ++i, ++L) {
                 const int s = L % STAGES;
                 ok = wait_bounded(bar(C::B_FULL + s), (L / STAGES) & 1, abort_flag);
-                // one decision for all four warps: the named barriers below need them all
+                // one decision for all eight warps: the named barriers below need them all
                 if (named_bar_or(3, kComputeThreads, !ok || *abort_flag != 0)) {
                     ok = false;
                     break;
                 }
                 const uint32_t ktile = sbase + C::KV_OFF + (2 * s) * C::TILE;
                 const uint32_t vtile = ktile + C::TILE;
-                const int key = (t0 + i) * kTileKeys + r;
-                // ---- scores of key r against every query ----
-                float acc[kMaxNq];
+                const int key = (t0 + i) * kTileKeys + key_r;
+                // ---- scores: this thread's half of key key_r against every query ----
+                float2 acc[NQ];
 #pragma unroll
-                for (int qi = 0; qi < kMaxNq; ++qi)
-                    acc[qi] = 0.f;
-#pragma unroll 2
-                for (int c8 = 0; c8 < D / 8; ++c8) {
-                    float kf[8];
-                    load8<T>(ktile + sw128_offset(r, c8), kf);
+                for (int qi = 0; qi < NQ; ++qi)
+                    acc[qi] = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int qi = 0; qi < kMaxNq; ++qi) {
-                        if (qi < Nq) {
-                            const uint8_t *qa = smem + C::QF_OFF + 4 * (qi * D + 8 * c8);
-                            const float4 a = *reinterpret_cast<const float4 *>(qa);
-                            const float4 b = *reinterpret_cast<const float4 *>(qa + 16);
-                            acc[qi] = fmaf(a.x, kf[0], acc[qi]);
-                            acc[qi] = fmaf(a.y, kf[1], acc[qi]);
-                            acc[qi] = fmaf(a.z, kf[2], acc[qi]);
-                            acc[qi] = fmaf(a.w, kf[3], acc[qi]);
-                            acc[qi] = fmaf(b.x, kf[4], acc[qi]);
-                            acc[qi] = fmaf(b.y, kf[5], acc[qi]);
-                            acc[qi] = fmaf(b.z, kf[6], acc[qi]);
-                            acc[qi] = fmaf(b.w, kf[7], acc[qi]);
-                        }
+                for (int c = 0; c < HALF_CHUNKS; ++c) {
+                    const int chunk = half * HALF_CHUNKS + c;  // 16-byte chunk of the row
+                    const uint32_t addr = ktile + static_cast<uint32_t>((chunk >> 3) * kSwAtomBytes) + krow +
+                                          ((static_cast<uint32_t>((chunk & 7) ^ (key_r & 7))) << 4);
+                    const uint4 kx = ld_shared_v4(addr);
+                    const float2 k0 = DTypeTraits<T>::unpack(kx.x), k1 = DTypeTraits<T>::unpack(kx.y);
+                    const float2 k2 = DTypeTraits<T>::unpack(kx.z), k3 = DTypeTraits<T>::unpack(kx.w);
+#pragma unroll
+                    for (int qi = 0; qi < NQ; ++qi) {
+                        const float4 a = *reinterpret_cast<const float4 *>(smem + C::QF_OFF + 4 * (qi * D + 8 * chunk));
+                        const float4 b = *reinterpret_cast<const float4 *>(smem + C::QF_OFF + 4 * (qi * D + 8 * chunk + 4));
+                        acc[qi] = ffma2(make_float2(a.x, a.y), k0, acc[qi]);
+                        acc[qi] = ffma2(make_float2(a.z, a.w), k1, acc[qi]);
+                        acc[qi] = ffma2(make_float2(b.x, b.y), k2, acc[qi]);
+                        acc[qi] = ffma2(make_float2(b.z, b.w), k3, acc[qi]);
                     }
                 }
-                // ---- masks, tile maxima ----
+                // ---- both halves, masks, tile maxima ----
+                float sc[NQ];
 #pragma unroll
-                for (int qi = 0; qi < kMaxNq; ++qi) {
-                    if (qi < Nq) {
-                        const int last = causal ? Nk - Nq + qi : Nk - 1;  // last key query qi may see
-                        if (key > last)
-                            acc[qi] = -INFINITY;
-                        float wm = acc[qi];
+                for (int qi = 0; qi < NQ; ++qi) {
+                    float v = acc[qi].x + acc[qi].y;
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    const int last = causal ? Nk - Nq + qi : Nk - 1;  // last key query qi may see
+                    if (key > last)
+                        v = -INFINITY;
+                    sc[qi] = v;
+                    float wm = v;
 #pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
-                        if (lane == 0)
-                            st_shared_f32(sbase + C::WM_OFF + 4u * (qi * 4 + warp), wm);
-                    }
+                    for (int off = 16; off > 1; off >>= 1)
+                        wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+                    if (lane == 0)
+                        st_shared_f32(sbase + C::WM_OFF + 4u * (qi * kComputeWarps + warp), wm);
                 }
                 named_bar_sync(1, kComputeThreads);
-                float alpha[kMaxNq];
+                float alpha[NQ];
 #pragma unroll
-                for (int qi = 0; qi < kMaxNq; ++qi) {
+                for (int qi = 0; qi < NQ; ++qi) {
+                    const float4 w0 = *reinterpret_cast<const float4 *>(smem + C::WM_OFF + 4 * (qi * kComputeWarps));
+                    const float4 w1 = *reinterpret_cast<const float4 *>(smem + C::WM_OFF + 4 * (qi * kComputeWarps + 4));
+                    const float tmax = fmaxf(fmax3(w0.x, w0.y, w0.z), fmax3(fmax3(w0.w, w1.x, w1.y), w1.z, w1.w));
+                    const float m_new = fmaxf(m[qi], tmax);
+                    float p = 0.f;
                     alpha[qi] = 1.f;
-                    if (qi < Nq) {
-                        const uint32_t wa = sbase + C::WM_OFF + 4u * (qi * 4);
-                        const float tmax = fmaxf(fmaxf(ld_shared_f32(wa), ld_shared_f32(wa + 4)),
-                                                 fmaxf(ld_shared_f32(wa + 8), ld_shared_f32(wa + 12)));
-                        const float m_new = fmaxf(m[qi], tmax);
-                        float p = 0.f;
-                        if (m_new != -INFINITY) {  // some key of this query seen so far
-                            alpha[qi] = ex2_approx(m[qi] - m_new);
-                            p = ex2_approx(acc[qi] - m_new);
-                            m[qi] = m_new;
-                        }
+                    if (m_new != -INFINITY) {  // some key of this query seen so far
+                        alpha[qi] = ex2_approx(m[qi] - m_new);
+                        p = ex2_approx(sc[qi] - m_new);
+                        m[qi] = m_new;
+                    }
+                    if (half == 0) {
                         l[qi] = l[qi] * alpha[qi] + p;
-                        st_shared_f32(sbase + C::PS_OFF + 4u * (qi * kTileKeys + r), p);
+                        st_shared_f32(sbase + C::PS_OFF + 4u * (qi * kTileKeys + key_r), p);
                     }
                 }
                 named_bar_sync(1, kComputeThreads);
                 // ---- P V: column pair `pair`, keys [grp KEYS_PER_GROUP, +KEYS_PER_GROUP) ----
-                const int c8 = (2 * pair) >> 3;
-                const uint32_t in_chunk = static_cast<uint32_t>((2 * pair) & 7) * 2u;
 #pragma unroll
-                for (int qi = 0; qi < kMaxNq; ++qi)
-                    if (qi < Nq)
-                        o[qi] = make_float2(o[qi].x * alpha[qi], o[qi].y * alpha[qi]);
-#pragma unroll 4
-                for (int jj = 0; jj < KEYS_PER_GROUP; ++jj) {
-                    const int j = grp * KEYS_PER_GROUP + jj;
-                    const float2 vv = DTypeTraits<T>::unpack(ld_shared_u32(vtile + sw128_offset(j, c8) + in_chunk));
+                for (int qi = 0; qi < NQ; ++qi)
+                    o[qi] = fmul2(o[qi], make_float2(alpha[qi], alpha[qi]));
+                const uint32_t vbase = vtile + pv_col + static_cast<uint32_t>(grp * C::KEYS_PER_GROUP) * 128u;
+                const uint8_t *pbase = smem + C::PS_OFF + 4 * (grp * C::KEYS_PER_GROUP);
 #pragma unroll
-                    for (int qi = 0; qi < kMaxNq; ++qi) {
-                        if (qi < Nq) {
-                            const float p = ld_shared_f32(sbase + C::PS_OFF + 4u * (qi * kTileKeys + j));
-                            o[qi] = make_float2(fmaf(p, vv.x, o[qi].x), fmaf(p, vv.y, o[qi].y));
+                for (int j4 = 0; j4 < C::KEYS_PER_GROUP; j4 += 4) {
+                    float4 pq[NQ];
+#pragma unroll
+                    for (int qi = 0; qi < NQ; ++qi)
+                        pq[qi] = *reinterpret_cast<const float4 *>(pbase + 4 * (qi * kTileKeys + j4));
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int jj = j4 + u;  // key of the group; its row % 8 is jj % 8
+                        const uint32_t va = vbase + static_cast<uint32_t>(jj) * 128u +
+                                            ((static_cast<uint32_t>((pc8 & 7) ^ (jj & 7))) << 4);
+                        const float2 vv = DTypeTraits<T>::unpack(ld_shared_u32(va));
+#pragma unroll
+                        for (int qi = 0; qi < NQ; ++qi) {
+                            const float pj = u == 0 ? pq[qi].x : u == 1 ? pq[qi].y : u == 2 ? pq[qi].z : pq[qi].w;
+                            o[qi] = ffma2(make_float2(pj, pj), vv, o[qi]);
                         }
                     }
                 }
@@ -300,38 +332,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok)
                 break;
             // ---------------- the item's (m, l, O) ----------------
-            // l: sum over the 128 threads (keys); O: sum over the key groups
+            // l: sum over the threads (keys); O: sum over the key groups
 #pragma unroll
-            for (int qi = 0; qi < kMaxNq; ++qi) {
-                if (qi < Nq) {
-                    float ws = l[qi];
+            for (int qi = 0; qi < NQ; ++qi) {
+                float ws = l[qi];
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        ws += __shfl_xor_sync(0xffffffffu, ws, off);
-                    if (lane == 0)
-                        st_shared_f32(sbase + C::WM_OFF + 4u * (qi * 4 + warp), ws);
-                    const uint32_t oa = sbase + C::RO_OFF + 4u * ((grp * kMaxNq + qi) * D + 2 * pair);
-                    st_shared_f32(oa, o[qi].x);
-                    st_shared_f32(oa + 4, o[qi].y);
-                }
+                for (int off = 16; off > 0; off >>= 1)
+                    ws += __shfl_xor_sync(0xffffffffu, ws, off);
+                if (lane == 0)
+                    st_shared_f32(sbase + C::WM_OFF + 4u * (qi * kComputeWarps + warp), ws);
+                const uint32_t oa = sbase + C::RO_OFF + 4u * ((grp * NQ + qi) * D + 2 * pair);
+                st_shared_f32(oa, o[qi].x);
+                st_shared_f32(oa + 4, o[qi].y);
             }
             named_bar_sync(1, kComputeThreads);
             const size_t base = (static_cast<size_t>(bh) * splits + split) * Nq;
-            for (int x = r; x < Nq * D; x += kComputeThreads) {
+            for (int x = t; x < Nq * D; x += kComputeThreads) {
                 const int qi = x / D, c = x % D;
                 float sum = 0.f;
                 for (int g = 0; g < C::GROUPS; ++g)
-                    sum += ld_shared_f32(sbase + C::RO_OFF + 4u * ((g * kMaxNq + qi) * D + c));
+                    sum += ld_shared_f32(sbase + C::RO_OFF + 4u * ((g * NQ + qi) * D + c));
                 part.o[(base + qi) * D + c] = sum;
             }
-            if (r < Nq) {
-                const uint32_t wa = sbase + C::WM_OFF + 4u * (r * 4);
-                part.l[base + r] = ld_shared_f32(wa) + ld_shared_f32(wa + 4) + ld_shared_f32(wa + 8) +
-                                   ld_shared_f32(wa + 12);
+            if (t < Nq) {
+                float sum = 0.f;
+                for (int wi = 0; wi < kComputeWarps; ++wi)
+                    sum += ld_shared_f32(sbase + C::WM_OFF + 4u * (t * kComputeWarps + wi));
+                part.l[base + t] = sum;
 #pragma unroll
-                for (int qi = 0; qi < kMaxNq; ++qi)
-                    if (qi == r)
-                        part.m[base + r] = m[qi];
+                for (int qi = 0; qi < NQ; ++qi)
+                    if (qi == t)
+                        part.m[base + t] = m[qi];
             }
             // every read of the reduction areas and of q is done before the next item
             named_bar_sync(1, kComputeThreads);

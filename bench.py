@@ -15,6 +15,12 @@ clocks (nvidia-smi sampled during warm-up + timed region), gpu_launches.
 --impl reference times the fp64 CPU oracle (the reference arm of this build)
 on a bounded row sample of the same workload, on the host cores.
 
+--op decode measures decoding attention (fa_decode: Nq <= 16 query rows per
+head against a long KV sequence, split-KV) on a decoding workload
+(--workload decode or decode_spec); it is HBM-bound, so its metric and
+roofline are the bytes of K and V streamed per second against the measured
+HBM bandwidth.
+
 --op bwd measures the backward pass instead (fa_bwd: gradients of Q, K, V from
 the forward's O and LSE and an upstream gradient dO), FLOPs = 2.5x the
 forward's (five N x N x d products per head instead of two); its CPU legs time
@@ -40,6 +46,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
 METRIC_BWD = "attention bwd TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
+METRIC_DEC = "decoding attention K/V GB/s at 1 GB300 and % of measured HBM bandwidth"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -50,8 +57,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="base")
-    ap.add_argument("--op", choices=["fwd", "bwd"], default="fwd",
-                    help="fwd: the attention forward (the default step); bwd: the backward pass")
+    ap.add_argument("--op", choices=["fwd", "bwd", "decode"], default="fwd",
+                    help="fwd: the attention forward (the default step); bwd: the backward pass; "
+                         "decode: decoding attention (use --workload decode / decode_spec)")
     ap.add_argument("--kernel", choices=["fa2", "fa1"], default="fa2",
                     help="fa2: the tiled FA2 forward (the product); fa1: the FA1-structured "
                          "baseline the pages compare it against")
@@ -93,6 +101,7 @@ KERNEL_SOURCES = {
     "fa1": ("fa_fwd.cu", "fa_fwd_kernel.cuh", "fa1_fwd_kernel.cuh", "fa_common.cuh", "fa_host.h",
             "sm100_ptx.cuh"),
     "bwd": ("fa_bwd.cu", "fa_bwd_kernel.cuh", "fa_common.cuh", "fa_host.h", "sm100_ptx.cuh"),
+    "decode": ("fa_decode.cu", "fa_decode_kernel.cuh", "fa_common.cuh", "fa_host.h", "sm100_ptx.cuh"),
 }
 
 
@@ -108,7 +117,7 @@ def kernel_source_hash(kernel="fa2"):
 def recorded_traffic(workload, src_hash, kernel="fa2"):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, valid only while the kernel sources are the ones profiled."""
-    stem = {"fa2": "fa_fwd", "fa1": "fa1_fwd", "bwd": "fa_bwd"}[kernel]
+    stem = {"fa2": "fa_fwd", "fa1": "fa1_fwd", "bwd": "fa_bwd", "decode": "fa_decode"}[kernel]
     path = os.path.join(ROOT, "profiles", "%s_%s_dram.md" % (stem, workload))
     try:
         text = open(path).read()
@@ -356,6 +365,8 @@ def main():
     from attention_forward_02_gb300 import inputs
 
     world, rank, local = dist_env()
+    if args.op == "decode":
+        return run_decode_op(args, world, rank, local)
     variants = [v.strip() == "causal" for v in args.variants.split(",") if v.strip()]
     q, k, v, meta = inputs.make_workload(args.workload)
     meta["name"] = args.workload
@@ -769,6 +780,226 @@ def run_reference_bwd(args, q, k, v, do, meta, variants, config, world, rank):
                                        "sample": sample},
                       "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                               "d2h_bytes_per_step": 0}}), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# decoding
+
+
+def decode_bytes(meta):
+    """Algorithmic bytes of one decoding call: K and V once, Q in, O out (16-bit), LSE (fp32)."""
+    BH, Nq, Nk, d = meta["B"] * meta["H"], meta["Nq"], meta["Nk"], meta["d"]
+    return BH * (2 * Nk * d * 2 + 2 * Nq * d * 2 + Nq * 4)
+
+
+def decode_flops(meta):
+    BH, Nq, Nk, d = meta["B"] * meta["H"], meta["Nq"], meta["Nk"], meta["d"]
+    if meta["causal"]:
+        keys = sum(Nk - Nq + i + 1 for i in range(Nq))
+        return 4.0 * BH * keys * d
+    return 4.0 * BH * Nq * Nk * d
+
+
+class OracleDecodeTimer:
+    """Times the fp64 oracle's decoding definition (as it stands) on whole heads."""
+
+    def __init__(self, q, k, v, meta):
+        import oracle
+        self.orc = oracle.get()
+        self.meta = meta
+        B, H = meta["B"], meta["H"]
+        self.q64 = q.double().numpy().reshape(B * H, 1, meta["Nq"], meta["d"])
+        self.k64 = k.double().numpy().reshape(B * H, 1, meta["Nk"], meta["d"])
+        self.v64 = v.double().numpy().reshape(B * H, 1, meta["Nk"], meta["d"])
+        self.threads = self.orc.default_threads()
+
+    def run(self, heads):
+        import numpy as np
+        sel = np.asarray(heads, dtype=np.int64)
+        t0 = time.perf_counter()
+        self.orc.attention_decode(self.q64[sel].reshape(1, len(sel), self.meta["Nq"], self.meta["d"]),
+                                  self.k64[sel].reshape(1, len(sel), self.meta["Nk"], self.meta["d"]),
+                                  self.v64[sel].reshape(1, len(sel), self.meta["Nk"], self.meta["d"]),
+                                  self.meta["d"] ** -0.5, causal=self.meta["causal"], threads=self.threads)
+        dt = time.perf_counter() - t0
+        one = dict(self.meta, B=1, H=len(sel))
+        return dt, decode_bytes(one)
+
+    def heads_for_seconds(self, seconds):
+        total = self.meta["B"] * self.meta["H"]
+        n = min(total, 4 * self.threads)
+        dt, _ = self.run(list(range(n)))
+        return max(1, min(total, int(seconds / max(dt / n, 1e-9))))
+
+    def threads_used(self, n_rows):
+        return min(self.threads, n_rows)
+
+
+def run_decode_op(args, world, rank, local):
+    from attention_forward_02_gb300 import inputs
+    name = args.workload if args.workload in inputs.DECODE_WORKLOADS else "decode"
+    q, k, v, meta = inputs.make_decode_workload(name)
+    meta["name"] = name
+    B, H, Nq, Nk, d = meta["B"], meta["H"], meta["Nq"], meta["Nk"], meta["d"]
+    config = {"workload": "%s B=%d H=%d Nq=%d Nk=%d d=%d %s %s" % (
+                  name, B, H, Nq, Nk, d, meta["dtype"], "causal (queries at the end)" if meta["causal"]
+                  else "non-causal"),
+              "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "scale": "1/sqrt(d)",
+              "inputs": "seeded iid N(0,1), rounded to %s" % meta["dtype"],
+              "l2": "flushed between timed steps (256 MiB write); K/V (%.2f GB) also exceed L2"
+                    % (2 * B * H * Nk * d * 2 / 1e9),
+              "parallelism": "dp%d (independent replicas)" % max(world, args.gpus),
+              "op": "decoding attention (split-KV)", "kernel": "fa_decode"}
+    step_bytes = decode_bytes(meta)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        timer = OracleDecodeTimer(q, k, v, meta)
+        n_steps = args.steps + max(args.warmup, 0)
+        heads = timer.heads_for_seconds(max(0.5, args.ref_seconds) / max(n_steps, 1))
+        total = B * H
+        for i in range(max(args.warmup, 0)):
+            timer.run([(i * heads + h) % total for h in range(heads)])
+        tot_t, tot_b = 0.0, 0.0
+        for i in range(args.steps):
+            dt, by = timer.run([((i + args.warmup) * heads + h) % total for h in range(heads)])
+            tot_t += dt
+            tot_b += by
+        value = tot_b / tot_t / 1e9
+        sample = "each step: %d of %d heads of %s, fp64 C oracle" % (heads, total, name)
+        print(json.dumps({"impl": "reference", "metric": METRIC_DEC, "value": value, "unit": "GB/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": config,
+                          "cpu_baseline": {"value": value, "unit": "GB/s",
+                                           "cores": timer.threads_used(heads * Nq), "kind": "oracle",
+                                           "sample": sample},
+                          "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    import torch
+    import attention_forward_02_gb300 as fa
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product has no CPU path)")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    fa.load()
+    scale = d ** -0.5
+    stream = torch.cuda.current_stream(dev)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_size(B, H, Nq, Nk, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def call(qq, oo, ll):
+        fa.fa_decode(qq, kd, vd, o=oo, lse=ll, scale=scale, causal=meta["causal"], workspace=ws,
+                     stream=stream)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    t_load0 = time.time()
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        call(qd, o, lse)
+    torch.cuda.synchronize(dev)
+    st = fa.fa_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise SystemExit("device status after warm-up: %s" % fa.fa_status_str(st))
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(2_000_000)
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        call(qd, o, lse)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    sampler.mark_load(t_load0, time.time())
+    st = fa.fa_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise SystemExit("device status after timed region: %s" % fa.fa_status_str(st))
+    ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(dist, sum(ms), dev)
+    value = sum_over_ranks(dist, step_bytes * K, dev) / (total_ms / 1e3) / 1e9
+
+    # e2e: per step the new queries go host -> device and O, LSE come back;
+    # the KV cache is device-resident state, as in a decoding loop
+    e2e = None
+    if not args.no_e2e:
+        hq = q.pin_memory()
+        ho = torch.empty_like(hq).pin_memory()
+        hl = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+        qq = torch.empty_like(qd)
+        steps_e = max(3, min(K, 50))
+
+        def one():
+            qq.copy_(hq, non_blocking=True)
+            call(qq, o, lse)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps_e):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+        e2e = {"value": sum_over_ranks(dist, step_bytes * steps_e, dev) / (ems / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hq.numel() * hq.element_size(),
+               "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * 4,
+               "steps": steps_e, "ms_per_step": ems / steps_e,
+               "note": "KV cache resident on the device (decoding state), queries in and O/LSE out per step"}
+    clocks = sampler.stop()
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    launch_ms = statistics.mean(ms)
+    achieved = step_bytes / (launch_ms / 1e3) / 1e9
+    traffic, _ = recorded_traffic(name, kernel_source_hash("decode"), "decode")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic,
+                "kernel": "fa_decode_split_kernel<%d,%s> + combine" % (d, meta["dtype"]),
+                "timed": "the whole fa_decode call (split kernel + combine kernel)",
+                "peak_source": "%s hbm_gbs (STREAM-style copy)" % peak_src,
+                "launch_ms": launch_ms, "algorithmic_bytes_per_launch": step_bytes,
+                "tflops": decode_flops(meta) / (launch_ms / 1e3) / 1e12}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        timer = OracleDecodeTimer(q, k, v, meta)
+        n = timer.heads_for_seconds(args.cpu_seconds)
+        dt, by = timer.run(list(range(n)))
+        cpu = {"value": by / dt / 1e9, "unit": "GB/s", "cores": timer.threads_used(n * Nq), "kind": "oracle",
+               "sample": "%d of %d heads of workload %s, fp64 C oracle, %.1f s" % (n, B * H, name, dt)}
+    if rank == 0:
+        print(json.dumps({"metric": METRIC_DEC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+                          "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "pct_of_peak": 100.0 * value / peak,
+                          "dtype": meta["dtype"], "data": "synthetic", "config": config,
+                          "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                          "gpu_launches": 2 * K, "wall_s_timed": t_wall}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":
