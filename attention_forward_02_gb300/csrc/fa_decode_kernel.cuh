@@ -27,7 +27,9 @@
 //
 // Warp roles of the split kernel (288 threads): warps 0-7 compute, warp 8 TMA
 // producer.  Per tile and query:
-//   scores   threads 2r, 2r + 1 take key r of the tile, half of d each:
+//   scores   lanes l and l + 16 of warp w take key 16 w + l of the tile, half
+//            of d each (so every 8-lane quarter of a 128-bit shared load reads
+//            8 consecutive rows: no bank conflict under the 128B swizzle):
 //            s' = (q scale log2 e) . k_r in packed fp32 FMAs, halves summed by
 //            a lane shuffle;
 //   max      warp shuffles, then the eight warps' maxima through shared memory;
@@ -191,8 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------- compute warps ----------------
         const int t = threadIdx.x;
-        const int key_r = t >> 1;           // score phase: key of the tile ...
-        const int half = t & 1;             // ... and which half of d
+        const int key_r = warp * 16 + (lane & 15);  // score phase: key of the tile ...
+        const int half = lane >> 4;                 // ... and which half of d
         const int pair = t % C::PAIRS;      // P V phase: column pair ...
         const int grp = t / C::PAIRS;       // ... and key group
         // score phase: byte offset of 16-byte chunk c of this thread's half row
@@ -266,14 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int qi = 0; qi < NQ; ++qi) {
                     float v = acc[qi].x + acc[qi].y;
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
                     const int last = causal ? Nk - Nq + qi : Nk - 1;  // last key query qi may see
                     if (key > last)
                         v = -INFINITY;
                     sc[qi] = v;
                     float wm = v;
 #pragma unroll
-                    for (int off = 16; off > 1; off >>= 1)
+                    for (int off = 8; off > 0; off >>= 1)  // lanes l, l + 16 hold the same score
                         wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
                     if (lane == 0)
                         st_shared_f32(sbase + C::WM_OFF + 4u * (qi * kComputeWarps + warp), wm);
