@@ -133,6 +133,8 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     bool empty = false;
     // q, k, v, o as in the forward (o is an input here; the overlap check
     // against q, k, v still applies: they are distinct tensors)
+    if (d != 64 && d != 128 && B >= 0 && H >= 0 && N >= 0)
+        return FA_ERR_UNSUPPORTED;  // the backward kernel is built for head dims 64 and 128
     fa_status_t s = fa_host::check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
     if (s != FA_OK || empty)
         return s;

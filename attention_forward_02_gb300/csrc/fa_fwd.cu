@@ -66,6 +66,14 @@ void init_device(int dev, DeviceState &st)
     }
     st.encode = reinterpret_cast<EncodeTiledFn>(fn);
     cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = set_smem_attr<32, false, __half>();
+    if (e == cudaSuccess) e = set_smem_attr<32, true, __half>();
+    if (e == cudaSuccess) e = set_smem_attr<96, false, __half>();
+    if (e == cudaSuccess) e = set_smem_attr<96, true, __half>();
+    if (e == cudaSuccess) e = set_smem_attr<32, false, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr<32, true, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr<96, false, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr<96, true, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr<64, false, __half>();
     if (e == cudaSuccess) e = set_smem_attr<64, true, __half>();
     if (e == cudaSuccess) e = set_smem_attr<128, false, __half>();
@@ -100,6 +108,23 @@ fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorM
     fa::fa_fwd_kernel<D, CAUSAL, T><<<grid, fa::kNumThreads, fa::KCfg<D>::SMEM_ALLOC, stream>>>(
         mq, mk, mv, static_cast<T *>(o), lse, N, BH, num_q_blocks, scale, scale_log2);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Head-dim and causal dispatch of the FA2 launch.
+template <typename T>
+fa_status_t launch_d(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o, float *lse,
+                     int BH, int N, int d, float scale, int causal, int num_sms, cudaStream_t stream)
+{
+#define FA_LAUNCH_D(DD)                                                                                  \
+    if (d == DD)                                                                                         \
+        return causal ? launch<DD, true, T>(mq, mk, mv, o, lse, BH, N, scale, num_sms, stream)           \
+                      : launch<DD, false, T>(mq, mk, mv, o, lse, BH, N, scale, num_sms, stream);
+    FA_LAUNCH_D(32)
+    FA_LAUNCH_D(64)
+    FA_LAUNCH_D(96)
+    FA_LAUNCH_D(128)
+#undef FA_LAUNCH_D
+    return FA_ERR_UNSUPPORTED;
 }
 
 template <int D, bool CAUSAL, typename T>
@@ -166,7 +191,7 @@ fa_status_t check_args(const void *q, const void *k, const void *v, const void *
         return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16)
         return FA_ERR_UNSUPPORTED;
-    if (d != 64 && d != 128)
+    if (d != 32 && d != 64 && d != 96 && d != 128)
         return FA_ERR_UNSUPPORTED;
     if (scale < 0.f)
         return FA_ERR_UNSUPPORTED;
@@ -279,18 +304,8 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
     if ((s = prepare(q, k, v, bh, N, d, dtype, &mq, &mk, &mv, &sms)) != FA_OK)
         return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (dtype == FA_FP16) {
-        if (d == 64)
-            return causal ? launch<64, true, __half>(mq, mk, mv, o, lse, bh, N, scale, sms, cs)
-                          : launch<64, false, __half>(mq, mk, mv, o, lse, bh, N, scale, sms, cs);
-        return causal ? launch<128, true, __half>(mq, mk, mv, o, lse, bh, N, scale, sms, cs)
-                      : launch<128, false, __half>(mq, mk, mv, o, lse, bh, N, scale, sms, cs);
-    }
-    if (d == 64)
-        return causal ? launch<64, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, sms, cs)
-                      : launch<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, sms, cs);
-    return causal ? launch<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, sms, cs)
-                  : launch<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, bh, N, scale, sms, cs);
+    return dtype == FA_FP16 ? launch_d<__half>(mq, mk, mv, o, lse, bh, N, d, scale, causal, sms, cs)
+                            : launch_d<__nv_bfloat16>(mq, mk, mv, o, lse, bh, N, d, scale, causal, sms, cs);
 }
 
 size_t fa1_fwd_workspace_size(int B, int H, int N, int d)
@@ -308,6 +323,8 @@ fa_status_t fa1_fwd(const void *q, const void *k, const void *v, void *o, float 
     fa_status_t s = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
     if (s != FA_OK || empty)
         return s;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;  // the FA1 baseline is built for the pages' head dims
     const size_t need = fa1_fwd_workspace_size(B, H, N, d);
     if (!workspace || workspace_bytes < need)
         return FA_ERR_INVALID_ARG;
@@ -350,6 +367,8 @@ fa_status_t fa1_fwd_noalloc(const void *q, const void *k, const void *v, void *o
     fa_status_t s = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
     if (s != FA_OK || empty)
         return s;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;
     if (fa1_fwd_workspace_size(B, H, N, d) > kNoAllocScratchBytes)
         return FA_ERR_UNSUPPORTED;  // problem needs more scratch than the fixed array holds
     int dev = -1;

@@ -63,27 +63,39 @@ constexpr uint32_t kRegsSoftmax = 200;
 constexpr uint32_t kRegsControl = 96;
 static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= 384 * 168, "register split");
 // TMEM columns: S0 @ 0, S1 @ 128, O0 @ 256, O1 @ 256 + D.  P_h (16-bit, two
-// per column) takes 64 columns: for D = 64 the spare columns 384 + 64 h, for
-// D = 128 the first half of S_h (the next S_h product is issued after the
+// per column) takes 64 columns: for D <= 64 the spare columns 256 + 2D + 64 h,
+// for D > 64 the first half of S_h (the next S_h product is issued after the
 // P_h V product that reads it, and tcgen05.mma ops of one thread execute in
 // issue order).
 constexpr uint32_t kTmemCols = 512;
 template <int D>
 __host__ __device__ constexpr uint32_t tmem_p_col(int h)
 {
-    return D == 64 ? 384u + 64u * h : 128u * h;
+    return D <= 64 ? 256u + 2u * D + 64u * h : 128u * h;
+}
+// Head dims 32 and 96 use the same tiles as 64 and 128: every row of a Q, K
+// or V tile is a whole number of 64-column (128-byte) swizzle blocks, and TMA
+// fills the columns past D with zeros (nothing past D is read from memory).
+// One 128-byte swizzle for every head dim, as "FlashAttention-2를 CuTe로
+// 밑바닥부터 구현하며 겪은 GPU 커널 지옥기" (section "V copy와 이상한 no-op
+// 이야기") suggests instead of a per-head-dim pattern.
+template <int D>
+__host__ __device__ constexpr int col_blocks()
+{
+    return (D + 63) / 64;
 }
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct KCfg {
-    static constexpr int TILE = 128 * D * 2;  // bytes of one [128, D] 16-bit tile
-    // D = 64: a 6-slot K/V ring and O staging tiles of their own, so the next
-    // item's Q can land while this item's output is stored.  D = 128: a 4-slot
+    static_assert(D == 32 || D == 64 || D == 96 || D == 128, "head dims 32, 64, 96, 128");
+    static constexpr int TILE = 128 * col_blocks<D>() * 128;  // bytes of one [128, D] 16-bit tile
+    // D <= 64: a 6-slot K/V ring and O staging tiles of their own, so the next
+    // item's Q can land while this item's output is stored.  D > 64: a 4-slot
     // ring; O is staged in the sub-tile's Q tile, which the next item's Q then
     // waits for (its items are long, so that wait matters little).
-    static constexpr bool STAGE_IN_Q = D == 128;
-    static constexpr int SLOTS = D == 64 ? 6 : 4;
+    static constexpr bool STAGE_IN_Q = D > 64;
+    static constexpr int SLOTS = D <= 64 ? 6 : 4;
     static constexpr int Q_OFF = 0;                      // Q0, Q1
     static constexpr int KV_OFF = Q_OFF + 2 * TILE;      // K/V ring
     static constexpr int OST_OFF = STAGE_IN_Q ? Q_OFF : KV_OFF + SLOTS * TILE;  // O staging
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // issued as soon as sub-tile h's softmax has finished with S_h,j, ahead of
     // P_h,j V_j, so the two softmax warpgroups need not wait for each other's
     // products.  With D = 128, P overwrites S_h, so S_h,j+1 follows P_h,j V_j.
-    constexpr bool EARLY_S = D == 64;
+    constexpr bool EARLY_S = D <= 64;
     constexpr int NUM_ISSUERS = EARLY_S ? 2 : 1;
     constexpr int SLOTS = C::SLOTS;
     constexpr int KSTEPS_QK = D / 16;  // UMMA_K = 16 for 16-bit operands
@@ -275,7 +287,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (it > 0 && !(ok = wait_bounded(bar(C::B_QEMPTY + h), (it - 1) & 1, abort_flag)))
                         break;
                     mbar_arrive_expect_tx(bar(C::B_QFULL + h), C::TILE);
-                    for (int b = 0; b < D / 64; ++b)
+                    for (int b = 0; b < col_blocks<D>(); ++b)
                         tma_load_3d(sbase + C::Q_OFF + h * C::TILE + b * kSwAtomBytes, &tm_q,
                                     bar(C::B_QFULL + h), b * 64, qb * kBM + h * kSubM, bh, pol_q);
                 }
@@ -289,7 +301,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     const CUtensorMap *map = (Ll & 1) ? &tm_v : &tm_k;
                     mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE);
-                    for (int b = 0; b < D / 64; ++b)
+                    for (int b = 0; b < col_blocks<D>(); ++b)
                         tma_load_3d(sbase + C::KV_OFF + s * C::TILE + b * kSwAtomBytes, map,
                                     bar(C::B_KVFULL + s), b * 64, (Ll >> 1) * kBN, bh, pol_kv);
                 }

@@ -33,6 +33,9 @@ WORKLOADS = {
     "sweep_b8": (8, 32, 2048, 64, "fp16", (50, 51, 52)),
     "d128": (2, 16, 8192, 128, "bf16", (30, 31, 32)),
     "long": (1, 8, 65536, 128, "fp16", (40, 41, 42)),
+    # head dims outside the pages' 64 / 128 (the base shape otherwise)
+    "hd32": (4, 32, 2048, 32, "fp16", (70, 71, 72)),
+    "hd96": (4, 32, 2048, 96, "fp16", (73, 74, 75)),
 }
 # seed of the upstream gradient dO per workload (backward pass)
 DOUT_SEEDS = {"tiny": 3, "base": 13, "sweep_b1": 33, "sweep_b2": 34, "sweep_b4": 35,

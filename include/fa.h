@@ -48,7 +48,7 @@ typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1, /* a NULL buffer, a negative size, causal not 0/1, a
                                non-finite scale, overlapping output and input */
-    FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, negative scale, dtype unknown,
+    FA_ERR_UNSUPPORTED = 2, /* d not supported, negative scale, dtype unknown,
                                N beyond the grid limit, device not sm_103 */
     FA_ERR_MISALIGNED = 3,  /* q, k, v or o not 16-byte aligned; lse not 4-byte */
     FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or the launch failed */
@@ -73,7 +73,8 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
  *  B, H, N : batch, heads, sequence length (queries = keys = N).  Any of them
  *            0 is an empty problem: FA_OK, nothing launched.  Ragged N (not a
  *            multiple of the 128-row tile) is supported.
- *  d       : head dimension, 64 or 128.
+ *  d       : head dimension, 32, 64, 96 or 128 (fa1_fwd, fa_bwd and fa_decode:
+ *            64 or 128).
  *  scale   : score scale (1/sqrt(d) for standard attention); finite, >= 0.
  *  causal  : 0 = every key; 1 = query i attends to keys j <= i.
  *  dtype   : FA_FP16 or FA_BF16.

@@ -59,7 +59,7 @@ def call(q=Q, k=K, v=V, o=O, lse=L, B=1, H=2, N=256, d=64, scale=0.125, causal=0
 
 
 @pytest.mark.parametrize("kwargs,status", [
-    (dict(d=96), 2), (dict(d=32), 2), (dict(d=256), 2),
+    (dict(d=48), 2), (dict(d=16), 2), (dict(d=256), 2),
     (dict(dtype=7), 2), (dict(scale=-1.0), 2),
     (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
     (dict(causal=2), 1), (dict(B=-1), 1), (dict(N=-5), 1),
@@ -93,7 +93,7 @@ def call_fa1(ws=W, ws_bytes=1 << 30, **kw):
 
 @pytest.mark.parametrize("kwargs,status", [
     (dict(ws=0), 1), (dict(ws_bytes=100), 1), (dict(ws=W + 8), 3), (dict(ws=Q), 1),
-    (dict(d=96), 2), (dict(causal=3), 1), (dict(N=0), 0),
+    (dict(d=96), 2), (dict(d=32), 2), (dict(causal=3), 1), (dict(N=0), 0),
 ], ids=lambda x: str(x))
 def test_fa1_argument_checks(lib, kwargs, status):
     assert call_fa1(**kwargs) == status
@@ -127,7 +127,8 @@ def call_bwd(ws=W, ws_bytes=1 << 30, **kw):
     (dict(dk=DQ + 64), 1),          # two outputs overlap
     (dict(dq=DO), 1),               # an output overlaps dout
     (dict(ws=L), 1),                # the workspace overlaps lse
-    (dict(d=96), 2), (dict(dtype=5), 2), (dict(causal=2), 1), (dict(scale=float("nan")), 1),
+    (dict(d=96), 2), (dict(d=32), 2), (dict(dtype=5), 2), (dict(causal=2), 1),
+    (dict(scale=float("nan")), 1),
     (dict(N=0), 0), (dict(B=0), 0),
 ], ids=lambda x: str(x))
 def test_bwd_argument_checks(lib, kwargs, status):

@@ -40,6 +40,28 @@ def test_ragged_lengths_full(orc, dtype, d, causal, N):
     check_full(orc, q, k, v, scale, causal, o, lse, "N=%d d=%d %s causal=%s" % (N, d, dtype, causal))
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("d", [32, 96])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 63, 129, 257, 640])
+def test_head_dims_32_96_full(orc, dtype, d, causal, N):
+    """Head dims 32 and 96: tiles of whole 64-column swizzle blocks whose
+    columns past d are zero-filled by TMA; products with K = d and N = d."""
+    q, k, v = inputs.make_qkv(2, 2, N, d, dtype, (3000 + N + d, 3100 + N, 3200 + d))
+    o, lse = run_gpu(q, k, v, d ** -0.5, causal)
+    check_full(orc, q, k, v, d ** -0.5, causal, o, lse, "N=%d d=%d %s causal=%s" % (N, d, dtype, causal))
+
+
+@pytest.mark.parametrize("name", ["hd32", "hd96"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_workloads_sampled(orc, name, causal):
+    q, k, v, meta = inputs.make_workload(name)
+    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+    o, lse = run_gpu(q, k, v, d ** -0.5, causal)
+    rows = edge_rows(B, H, N, inputs.sample_rows(B, H, N, 8, 4242))
+    check_rows(orc, q, k, v, d ** -0.5, causal, o, lse, rows, "%s causal=%s" % (name, causal))
+
+
 @pytest.mark.parametrize("d,dtype", [(64, "fp16"), (128, "bf16")])
 @pytest.mark.parametrize("causal", [False, True])
 def test_multi_head_multi_tile_full(orc, d, dtype, causal):
@@ -101,7 +123,7 @@ def test_empty_problem_writes_nothing(orc):
 def test_status_errors_on_device(orc):
     import attention_forward_02_gb300 as fa
     dev = torch.device("cuda:0")
-    x = torch.zeros(1, 1, 256, 96, dtype=torch.float16, device=dev)
+    x = torch.zeros(1, 1, 256, 48, dtype=torch.float16, device=dev)
     with pytest.raises(fa.FAError) as e:
         fa.fa_fwd(x, x, x)
     assert e.value.status == 2
