@@ -35,14 +35,16 @@ cudaError_t set_smem_attr()
 void init_bwd(BwdState &st)
 {
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem_attr<64, false, __half>();
-    if (e == cudaSuccess) e = set_smem_attr<64, true, __half>();
-    if (e == cudaSuccess) e = set_smem_attr<128, false, __half>();
-    if (e == cudaSuccess) e = set_smem_attr<128, true, __half>();
-    if (e == cudaSuccess) e = set_smem_attr<64, false, __nv_bfloat16>();
-    if (e == cudaSuccess) e = set_smem_attr<64, true, __nv_bfloat16>();
-    if (e == cudaSuccess) e = set_smem_attr<128, false, __nv_bfloat16>();
-    if (e == cudaSuccess) e = set_smem_attr<128, true, __nv_bfloat16>();
+#define FA_BWD_ATTR(DD)                                                                                   \
+    if (e == cudaSuccess) e = set_smem_attr<DD, false, __half>();                                         \
+    if (e == cudaSuccess) e = set_smem_attr<DD, true, __half>();                                          \
+    if (e == cudaSuccess) e = set_smem_attr<DD, false, __nv_bfloat16>();                                  \
+    if (e == cudaSuccess) e = set_smem_attr<DD, true, __nv_bfloat16>();
+    FA_BWD_ATTR(32)
+    FA_BWD_ATTR(64)
+    FA_BWD_ATTR(96)
+    FA_BWD_ATTR(128)
+#undef FA_BWD_ATTR
     st.err = e;
 }
 
@@ -77,7 +79,7 @@ fa_status_t launch(const Maps &mp, const void *o, const float *lse, const void *
     const int nb = static_cast<int>(Npad / kBlk);
     const long long rows = static_cast<long long>(BH) * Npad;
     {
-        const long long threads = rows * (D / 8);
+        const long long threads = rows * (D <= 32 ? 4 : D <= 64 ? 8 : 16);
         const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
         fa_bwd_prep_kernel<D, T><<<grid, 256, 0, stream>>>(static_cast<const T *>(o),
                                                             static_cast<const T *>(dout), lse, lse2, dvec,
@@ -120,7 +122,7 @@ extern "C" {
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d)
 {
-    if (B < 0 || H < 0 || N < 0 || (d != 64 && d != 128))
+    if (B < 0 || H < 0 || N < 0 || (d != 32 && d != 64 && d != 96 && d != 128))
         return 0;
     const size_t rows = static_cast<size_t>(B) * H * static_cast<size_t>(padded_rows(N));
     return rows * (static_cast<size_t>(d) + 2) * sizeof(float);
@@ -133,8 +135,6 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     bool empty = false;
     // q, k, v, o as in the forward (o is an input here; the overlap check
     // against q, k, v still applies: they are distinct tensors)
-    if (d != 64 && d != 128 && B >= 0 && H >= 0 && N >= 0)
-        return FA_ERR_UNSUPPORTED;  // the backward kernel is built for head dims 64 and 128
     fa_status_t s = fa_host::check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
     if (s != FA_OK || empty)
         return s;
@@ -194,16 +194,22 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 #define FA_BWD_ARGS mp, o, lse, dout, dq, acc, lse2, dvec, bh, N, scale, cs
+#define FA_BWD_D(DD, TT)                                                                                  \
+    if (d == DD)                                                                                          \
+        return causal ? launch<DD, true, TT>(FA_BWD_ARGS) : launch<DD, false, TT>(FA_BWD_ARGS);
     if (dtype == FA_FP16) {
-        if (d == 64)
-            return causal ? launch<64, true, __half>(FA_BWD_ARGS) : launch<64, false, __half>(FA_BWD_ARGS);
-        return causal ? launch<128, true, __half>(FA_BWD_ARGS) : launch<128, false, __half>(FA_BWD_ARGS);
+        FA_BWD_D(32, __half)
+        FA_BWD_D(64, __half)
+        FA_BWD_D(96, __half)
+        FA_BWD_D(128, __half)
+    } else {
+        FA_BWD_D(32, __nv_bfloat16)
+        FA_BWD_D(64, __nv_bfloat16)
+        FA_BWD_D(96, __nv_bfloat16)
+        FA_BWD_D(128, __nv_bfloat16)
     }
-    if (d == 64)
-        return causal ? launch<64, true, __nv_bfloat16>(FA_BWD_ARGS)
-                      : launch<64, false, __nv_bfloat16>(FA_BWD_ARGS);
-    return causal ? launch<128, true, __nv_bfloat16>(FA_BWD_ARGS)
-                  : launch<128, false, __nv_bfloat16>(FA_BWD_ARGS);
+    return FA_ERR_UNSUPPORTED;
+#undef FA_BWD_D
 #undef FA_BWD_ARGS
 }
 

@@ -52,11 +52,13 @@ constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S^T @ 0 (P^T, 16-bit, over its first columns), dP^T @ 128,
-// dV @ 256, dK @ 256 + D.  D = 64: dQ @ 384 and dS^T (16-bit) @ 448, so that
-// dP^T of the next query block can be computed while dK and dQ of this one
-// still read dS^T.  D = 128 (no spare columns): dS^T over the first dP^T
+// dV @ 256, dK @ 256 + D.  D <= 64: dQ @ 256 + 2D and dS^T (16-bit) @ 448, so
+// that dP^T of the next query block can be computed while dK and dQ of this
+// one still read dS^T.  D > 64 (no spare columns): dS^T over the first dP^T
 // columns and dQ_m over all of them, which the compute warps have finished
 // reading when dK and dQ_m are issued; the next dP^T waits for dQ_m to be read.
+// Head dims 32 and 96 use tiles of whole 64-column swizzle blocks (TMA fills
+// the columns past D with zeros), as the forward kernel does.
 constexpr uint32_t kTmS = 0;
 constexpr uint32_t kTmDP = 128;
 constexpr uint32_t kTmDV = 256;
@@ -68,12 +70,17 @@ __host__ __device__ constexpr uint32_t col_dk()
 template <int D>
 __host__ __device__ constexpr uint32_t col_dq()
 {
-    return D == 64 ? 384u : kTmDP;
+    return D <= 64 ? 256u + 2u * D : kTmDP;
 }
 template <int D>
 __host__ __device__ constexpr uint32_t col_ds()
 {
-    return D == 64 ? 448u : kTmDP;
+    return D <= 64 ? 448u : kTmDP;
+}
+template <int D>
+__host__ __device__ constexpr int col_blocks()
+{
+    return (D + 63) / 64;
 }
 // Column distance between the two compute warpgroups' halves of a 16-bit
 // P^T / dS^T tile (each half: 64 queries, two per column = 32 columns).  Over
@@ -83,7 +90,7 @@ __host__ __device__ constexpr uint32_t col_ds()
 template <int D>
 __host__ __device__ constexpr uint32_t ds_half()
 {
-    return D == 64 ? 32u : 64u;
+    return D <= 64 ? 32u : 64u;
 }
 static_assert(448u + 2 * 32u <= kTmemCols && 128u + 64u + 32u <= 256u, "dS^T columns inside their area");
 // TMEM column, relative to the start of the P^T or dS^T area, of K step t
@@ -97,12 +104,13 @@ __host__ __device__ constexpr uint32_t tm_p_step(int t, uint32_t half)
 
 template <int D>
 struct Cfg {
-    static constexpr int TILE = kBlk * D * 2;  // one [128, D] 16-bit tile
-    static constexpr int QST = D == 64 ? 3 : 2;   // Q (+ L) ring
-    static constexpr int DOST = D == 64 ? 3 : 1;  // dO (+ D) ring
-    static constexpr int NSTG = D == 64 ? 2 : 1;  // dQ staging buffers
+    static_assert(D == 32 || D == 64 || D == 96 || D == 128, "head dims 32, 64, 96, 128");
+    static constexpr int TILE = kBlk * col_blocks<D>() * 128;  // one [128, D] 16-bit tile
+    static constexpr int QST = D <= 64 ? 3 : 2;   // Q (+ L) ring
+    static constexpr int DOST = D <= 64 ? 3 : 1;  // dO (+ D) ring
+    static constexpr int NSTG = D <= 64 ? 2 : 1;  // dQ staging buffers
     static constexpr int STG_BYTES = kBlk * 32 * 4;  // [128 rows x 32 fp32], 128B-swizzled
-    static constexpr bool DQ_ALIAS = D == 128;  // dQ (and dS^T) over the dP^T columns
+    static constexpr bool DQ_ALIAS = D > 64;  // dQ (and dS^T) over the dP^T columns
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + TILE;
     static constexpr int Q_OFF = V_OFF + TILE;
@@ -220,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
             mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
-            for (int b = 0; b < D / 64; ++b) {
+            for (int b = 0; b < col_blocks<D>(); ++b) {
                 tma_load_3d(sbase + C::K_OFF + b * kSwAtomBytes, &tm_k, bar(C::B_KVFULL), b * 64, n * kBlk,
                             bh, pol_kv);
                 tma_load_3d(sbase + C::V_OFF + b * kSwAtomBytes, &tm_v, bar(C::B_KVFULL), b * 64, n * kBlk,
@@ -235,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i >= QST && !(ok = wait_bounded(bar(C::B_QEMPTY + s), ((i / QST) - 1) & 1, abort_flag)))
                     break;
                 mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE + kBlk * 4);
-                for (int b = 0; b < D / 64; ++b)
+                for (int b = 0; b < col_blocks<D>(); ++b)
                     tma_load_3d(sbase + C::Q_OFF + s * C::TILE + b * kSwAtomBytes, &tm_q, bar(C::B_QFULL + s),
                                 b * 64, m * kBlk, bh, pol_q);
                 bulk_load(sbase + C::L_OFF + s * kBlk * 4, lse2 + row0, kBlk * 4, bar(C::B_QFULL + s));
@@ -244,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i >= DOST && !(ok = wait_bounded(bar(C::B_DOEMPTY + ds), ((i / DOST) - 1) & 1, abort_flag)))
                     break;
                 mbar_arrive_expect_tx(bar(C::B_DOFULL + ds), C::TILE + kBlk * 4);
-                for (int b = 0; b < D / 64; ++b)
+                for (int b = 0; b < col_blocks<D>(); ++b)
                     tma_load_3d(sbase + C::DO_OFF + ds * C::TILE + b * kSwAtomBytes, &tm_do,
                                 bar(C::B_DOFULL + ds), b * 64, m * kBlk, bh, pol_q);
                 bulk_load(sbase + C::DD_OFF + ds * kBlk * 4, dvec + row0, kBlk * 4, bar(C::B_DOFULL + ds));
@@ -563,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             named_bar_sync(1 + c, 128);
             if (r == 0) {
-                for (int b = 0; b < D / 64; ++b)
+                for (int b = 0; b < col_blocks<D>(); ++b)
                     tma_store_3d(c == 0 ? &tm_dv : &tm_dk, stage + b * kSwAtomBytes, b * 64, n * kBlk, bh);
                 bulk_commit_group();
                 bulk_wait_group<0>();
@@ -591,7 +599,9 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const T *__restrict__ 
                                                           float *__restrict__ dqacc, int N, int Npad,
                                                           long long rows)
 {
-    constexpr int TPR = D / 8;
+    // threads per row: D / 8 rounded up to a power of two (so a row's threads
+    // sit in one warp); the parts past D have nothing to read
+    constexpr int TPR = D <= 32 ? 4 : D <= 64 ? 8 : 16;
     const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long row = g / TPR;
     const int part = static_cast<int>(g % TPR);
@@ -599,8 +609,9 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const T *__restrict__ 
     const long long bh = valid ? row / Npad : 0;
     const int i = valid ? static_cast<int>(row % Npad) : 0;
     const bool live = valid && i < N;
+    const bool has_part = part * 8 < D;
     float acc = 0.f;
-    if (live) {
+    if (live && has_part) {
         const size_t off = (static_cast<size_t>(bh) * N + i) * D + part * 8;
         const uint4 a = *reinterpret_cast<const uint4 *>(o + off);
         const uint4 b = *reinterpret_cast<const uint4 *>(dout + off);
@@ -622,9 +633,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const T *__restrict__ 
             dvec[row] = live ? acc : 0.f;
             lse2[row] = live ? lse[static_cast<size_t>(bh) * N + i] * 1.4426950408889634f : INFINITY;
         }
-        float4 *z = reinterpret_cast<float4 *>(dqacc + static_cast<size_t>(row) * D + part * 8);
-        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (has_part) {
+            float4 *z = reinterpret_cast<float4 *>(dqacc + static_cast<size_t>(row) * D + part * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
 }
 

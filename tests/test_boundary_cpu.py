@@ -104,7 +104,8 @@ def test_bwd_workspace_size(lib):
     assert fa.fa_bwd_workspace_size(4, 32, 2048, 64) == 4 * 32 * 2048 * 66 * 4
     assert fa.fa_bwd_workspace_size(1, 1, 1, 128) == 128 * 130 * 4
     assert fa.fa_bwd_workspace_size(2, 3, 200, 64) == 6 * 256 * 66 * 4
-    assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 128 * 98 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 48) == 0
     assert fa.fa_bwd_workspace_size(1, -1, 1, 64) == 0
 
 
@@ -127,7 +128,7 @@ def call_bwd(ws=W, ws_bytes=1 << 30, **kw):
     (dict(dk=DQ + 64), 1),          # two outputs overlap
     (dict(dq=DO), 1),               # an output overlaps dout
     (dict(ws=L), 1),                # the workspace overlaps lse
-    (dict(d=96), 2), (dict(d=32), 2), (dict(dtype=5), 2), (dict(causal=2), 1),
+    (dict(d=48), 2), (dict(dtype=5), 2), (dict(causal=2), 1),
     (dict(scale=float("nan")), 1),
     (dict(N=0), 0), (dict(B=0), 0),
 ], ids=lambda x: str(x))

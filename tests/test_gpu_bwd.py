@@ -45,6 +45,14 @@ def test_ragged(orc, dtype, d, causal, N):
     _case(orc, 1, 2, N, d, dtype, causal, 7000 + N)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("d", [32, 96])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 129, 384])
+def test_head_dims_32_96(orc, dtype, d, causal, N):
+    _case(orc, 1, 2, N, d, dtype, causal, 7300 + N + d)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_many_heads(orc, causal):
     _case(orc, 3, 3, 700, 64, "fp16", causal, 7100)
