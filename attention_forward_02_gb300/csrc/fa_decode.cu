@@ -46,9 +46,13 @@ cudaError_t set_smem_attr_all()
 void init_dec(DecState &st)
 {
     cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = set_smem_attr_all<32, __half>();
     if (e == cudaSuccess) e = set_smem_attr_all<64, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_all<96, __half>();
     if (e == cudaSuccess) e = set_smem_attr_all<128, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_all<32, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr_all<64, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_all<96, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr_all<128, __nv_bfloat16>();
     st.err = e;
 }
@@ -129,7 +133,7 @@ extern "C" {
 
 size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d)
 {
-    if (B < 0 || H < 0 || Nq < 1 || Nq > fa::dec::kMaxNq || Nk < Nq || (d != 64 && d != 128))
+    if (B < 0 || H < 0 || Nq < 1 || Nq > fa::dec::kMaxNq || Nk < Nq || (d != 32 && d != 64 && d != 96 && d != 128))
         return 0;
     // at most one chunk per key tile
     const size_t rows = static_cast<size_t>(B) * H * static_cast<size_t>(key_tiles(Nk)) * Nq;
@@ -148,7 +152,7 @@ fa_status_t fa_decode(const void *q, const void *k, const void *v, void *o, floa
         return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16)
         return FA_ERR_UNSUPPORTED;
-    if (d != 64 && d != 128)
+    if (d != 32 && d != 64 && d != 96 && d != 128)
         return FA_ERR_UNSUPPORTED;
     if (scale < 0.f)
         return FA_ERR_UNSUPPORTED;
@@ -205,11 +209,22 @@ fa_status_t fa_decode(const void *q, const void *k, const void *v, void *o, floa
     if ((s = fa_host::encode_qkv_map(encode, &mv, v, bh, Nk, d, dtype)) != FA_OK) return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     float *ws = static_cast<float *>(workspace);
-    if (dtype == FA_FP16)
-        return d == 64 ? launch<64, __half>(mk, mv, q, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs)
-                       : launch<128, __half>(mk, mv, q, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs);
-    return d == 64 ? launch<64, __nv_bfloat16>(mk, mv, q, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs)
-                   : launch<128, __nv_bfloat16>(mk, mv, q, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs);
+#define FA_DEC_D(DD, TT)                                                                                  \
+    if (d == DD)                                                                                          \
+        return launch<DD, TT>(mk, mv, q, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs);
+    if (dtype == FA_FP16) {
+        FA_DEC_D(32, __half)
+        FA_DEC_D(64, __half)
+        FA_DEC_D(96, __half)
+        FA_DEC_D(128, __half)
+    } else {
+        FA_DEC_D(32, __nv_bfloat16)
+        FA_DEC_D(64, __nv_bfloat16)
+        FA_DEC_D(96, __nv_bfloat16)
+        FA_DEC_D(128, __nv_bfloat16)
+    }
+#undef FA_DEC_D
+    return FA_ERR_UNSUPPORTED;
 }
 
 }  // extern "C"

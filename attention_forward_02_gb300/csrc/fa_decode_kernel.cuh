@@ -55,11 +55,22 @@ constexpr int kProducerWarp = kComputeWarps;
 constexpr int kThreads = kComputeThreads + 32;
 constexpr int kMaxNq = 16;
 
+// Head dims 32 and 96 use tiles of whole 64-column swizzle blocks (TMA fills
+// the columns past D with zeros), as the forward kernel does.
+template <int D>
+__host__ __device__ constexpr int col_blocks()
+{
+    return (D + 63) / 64;
+}
+
 template <int D, int NQ>
 struct Cfg {
-    static constexpr int TILE = kTileKeys * D * 2;   // one [128, D] 16-bit K or V tile
+    static_assert(D == 32 || D == 64 || D == 96 || D == 128, "head dims 32, 64, 96, 128");
+    static constexpr int TILE = kTileKeys * col_blocks<D>() * 128;  // one [128, D] 16-bit K or V tile
     static constexpr int PAIRS = D / 2;              // column pairs of the P V phase
-    static constexpr int GROUPS = kComputeThreads / PAIRS;  // key groups of the P V phase
+    // key groups of the P V phase (D = 96: 48 pairs x 4 groups, 64 threads idle there)
+    static constexpr int GROUPS = D == 96 ? 4 : kComputeThreads / PAIRS;
+    static constexpr int PV_THREADS = GROUPS * PAIRS;
     static constexpr int KEYS_PER_GROUP = kTileKeys / GROUPS;
     // per-CTA areas besides the ring (q, p, warp maxima, O reduction, barriers, slack)
     static constexpr int EXTRA = NQ * D * 4 + NQ * kTileKeys * 4 + NQ * kComputeWarps * 4 +
@@ -80,7 +91,9 @@ struct Cfg {
     static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // abort flag
     static constexpr int SMEM_USED = SLOT_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
-    static_assert(KEYS_PER_GROUP % 8 == 0, "key groups start on a swizzle period");
+    static_assert(KEYS_PER_GROUP % 8 == 0 && KEYS_PER_GROUP * GROUPS == kTileKeys,
+                  "key groups start on a swizzle period and cover the tile");
+    static_assert(PV_THREADS <= kComputeThreads, "P V threads");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -178,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     const uint32_t kdst = sbase + C::KV_OFF + (2 * s) * C::TILE;
                     mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE);
-                    for (int b = 0; b < D / 64; ++b) {
+                    for (int b = 0; b < col_blocks<D>(); ++b) {
                         tma_load_3d(kdst + b * kSwAtomBytes, &tm_k, bar(C::B_FULL + s), b * 64,
                                     (t0 + i) * kTileKeys, bh, pol);
                         tma_load_3d(kdst + C::TILE + b * kSwAtomBytes, &tm_v, bar(C::B_FULL + s), b * 64,
@@ -309,6 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t *pbase = smem + C::PS_OFF + 4 * (grp * C::KEYS_PER_GROUP);
 #pragma unroll
                 for (int j4 = 0; j4 < C::KEYS_PER_GROUP; j4 += 4) {
+                    if (C::PV_THREADS < kComputeThreads && t >= C::PV_THREADS)
+                        break;
                     float4 pq[NQ];
 #pragma unroll
                     for (int qi = 0; qi < NQ; ++qi)
@@ -343,9 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ws += __shfl_xor_sync(0xffffffffu, ws, off);
                 if (lane == 0)
                     st_shared_f32(sbase + C::WM_OFF + 4u * (qi * kComputeWarps + warp), ws);
-                const uint32_t oa = sbase + C::RO_OFF + 4u * ((grp * NQ + qi) * D + 2 * pair);
-                st_shared_f32(oa, o[qi].x);
-                st_shared_f32(oa + 4, o[qi].y);
+                if (t < C::PV_THREADS) {
+                    const uint32_t oa = sbase + C::RO_OFF + 4u * ((grp * NQ + qi) * D + 2 * pair);
+                    st_shared_f32(oa, o[qi].x);
+                    st_shared_f32(oa + 4, o[qi].y);
+                }
             }
             named_bar_sync(1, kComputeThreads);
             const size_t base = (static_cast<size_t>(bh) * splits + split) * Nq;
@@ -390,11 +407,13 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(Partials part, T
     float M = -INFINITY;
     for (int s = 0; s < splits; ++s)
         M = fmaxf(M, part.m[(bh * splits + s) * Nq + qi]);
-    constexpr int PER = D / 32;
-    float acc[PER];
+    // column pairs 2 pr, 2 pr + 1 for pr = lane, lane + 32, ... (< D / 2)
+    constexpr int PAIRS = D / 2;
+    constexpr int PPL = (PAIRS + 31) / 32;
+    float2 acc[PPL];
 #pragma unroll
-    for (int c = 0; c < PER; ++c)
-        acc[c] = 0.f;
+    for (int k = 0; k < PPL; ++k)
+        acc[k] = make_float2(0.f, 0.f);
     float L = 0.f;
     for (int s = 0; s < splits; ++s) {
         const size_t idx = (static_cast<size_t>(bh) * splits + s) * Nq + qi;
@@ -404,15 +423,21 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(Partials part, T
         const float w = ex2_approx(ms - M);
         L = fmaf(part.l[idx], w, L);
 #pragma unroll
-        for (int c = 0; c < PER; ++c)
-            acc[c] = fmaf(part.o[idx * D + lane * PER + c], w, acc[c]);
+        for (int k = 0; k < PPL; ++k) {
+            const int pr = lane + 32 * k;
+            if (pr < PAIRS) {
+                const float2 v = *reinterpret_cast<const float2 *>(part.o + idx * D + 2 * pr);
+                acc[k] = make_float2(fmaf(v.x, w, acc[k].x), fmaf(v.y, w, acc[k].y));
+            }
+        }
     }
     const float inv = 1.f / L;
-    T *dst = out + static_cast<size_t>(row) * D + lane * PER;
+    T *dst = out + static_cast<size_t>(row) * D;
 #pragma unroll
-    for (int c = 0; c < PER; c += 2) {
-        const uint32_t w = DTypeTraits<T>::pack(acc[c] * inv, acc[c + 1] * inv);
-        *reinterpret_cast<uint32_t *>(dst + c) = w;
+    for (int k = 0; k < PPL; ++k) {
+        const int pr = lane + 32 * k;
+        if (pr < PAIRS)
+            *reinterpret_cast<uint32_t *>(dst + 2 * pr) = DTypeTraits<T>::pack(acc[k].x * inv, acc[k].y * inv);
     }
     if (lse != nullptr && lane == 0)
         lse[row] = (M + __log2f(L)) * 0.6931471805599453f;

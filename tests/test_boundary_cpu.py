@@ -142,7 +142,8 @@ def test_decode_workspace_size(lib):
     assert fa.fa_decode_workspace_size(1, 1, 4, 129, 64) == 2 * 4 * 66 * 4
     assert fa.fa_decode_workspace_size(1, 1, 17, 1000, 64) == 0   # Nq > 16
     assert fa.fa_decode_workspace_size(1, 1, 4, 3, 64) == 0       # Nk < Nq
-    assert fa.fa_decode_workspace_size(1, 1, 1, 10, 96) == 0
+    assert fa.fa_decode_workspace_size(1, 1, 1, 10, 96) == 1 * 98 * 4
+    assert fa.fa_decode_workspace_size(1, 1, 1, 10, 48) == 0
 
 
 def call_decode(ws=W, ws_bytes=1 << 30, **kw):
@@ -154,7 +155,7 @@ def call_decode(ws=W, ws_bytes=1 << 30, **kw):
 
 @pytest.mark.parametrize("kwargs,status", [
     (dict(Nq=17), 2), (dict(Nq=0), 2), (dict(Nk=0), 1), (dict(Nq=4, Nk=3), 1),
-    (dict(d=96), 2), (dict(dtype=3), 2), (dict(causal=5), 1), (dict(scale=float("nan")), 1),
+    (dict(d=48), 2), (dict(dtype=3), 2), (dict(causal=5), 1), (dict(scale=float("nan")), 1),
     (dict(q=0), 1), (dict(ws=0), 1), (dict(ws_bytes=10), 1),
     (dict(k=K + 8), 3), (dict(lse=L + 1), 3), (dict(ws=W + 4), 3),
     (dict(o=K), 1), (dict(ws=V), 1),

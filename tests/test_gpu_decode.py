@@ -48,6 +48,15 @@ def test_small(orc, dtype, d, causal, Nq, Nk):
     check(orc, q, k, v, d ** -0.5, causal, "decode Nq%d Nk%d d%d %s causal=%s" % (Nq, Nk, d, dtype, causal))
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("d", [32, 96])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(1, 129), (3, 1000), (16, 4100)])
+def test_head_dims_32_96(orc, dtype, d, causal, Nq, Nk):
+    q, k, v = inputs.make_decode(2, 3, Nq, Nk, d, dtype, (9400 + Nk, 9500 + Nq, 9600 + d))
+    check(orc, q, k, v, d ** -0.5, causal, "decode Nq%d Nk%d d%d %s causal=%s" % (Nq, Nk, d, dtype, causal))
+
+
 def test_peaked_scores(orc):
     # q x 8: scaled scores with a standard deviation about 8 (the running max moves)
     q, k, v = inputs.make_decode(1, 4, 2, 5000, 128, "fp16", (9301, 9302, 9303))
