@@ -801,28 +801,32 @@ def decode_flops(meta):
 
 
 class OracleDecodeTimer:
-    """Times the fp64 oracle's decoding definition (as it stands) on whole heads."""
+    """Times the fp64 oracle's decoding definition (as it stands) on whole heads;
+    the sampled heads are widened to fp64 per call (a KV cache in fp64 would
+    not fit the host)."""
 
     def __init__(self, q, k, v, meta):
         import oracle
         self.orc = oracle.get()
         self.meta = meta
         B, H = meta["B"], meta["H"]
-        self.q64 = q.double().numpy().reshape(B * H, 1, meta["Nq"], meta["d"])
-        self.k64 = k.double().numpy().reshape(B * H, 1, meta["Nk"], meta["d"])
-        self.v64 = v.double().numpy().reshape(B * H, 1, meta["Nk"], meta["d"])
+        self.q = q.reshape(B * H, meta["Nq"], meta["d"])
+        self.k = k.reshape(B * H, meta["Nk"], meta["d"])
+        self.v = v.reshape(B * H, meta["Nk"], meta["d"])
         self.threads = self.orc.default_threads()
 
     def run(self, heads):
-        import numpy as np
-        sel = np.asarray(heads, dtype=np.int64)
+        import torch
+        sel = torch.as_tensor(list(heads), dtype=torch.long)
+        n = len(sel)
+        q64 = self.q[sel].double().numpy().reshape(1, n, self.meta["Nq"], self.meta["d"])
+        k64 = self.k[sel].double().numpy().reshape(1, n, self.meta["Nk"], self.meta["d"])
+        v64 = self.v[sel].double().numpy().reshape(1, n, self.meta["Nk"], self.meta["d"])
         t0 = time.perf_counter()
-        self.orc.attention_decode(self.q64[sel].reshape(1, len(sel), self.meta["Nq"], self.meta["d"]),
-                                  self.k64[sel].reshape(1, len(sel), self.meta["Nk"], self.meta["d"]),
-                                  self.v64[sel].reshape(1, len(sel), self.meta["Nk"], self.meta["d"]),
-                                  self.meta["d"] ** -0.5, causal=self.meta["causal"], threads=self.threads)
+        self.orc.attention_decode(q64, k64, v64, self.meta["d"] ** -0.5, causal=self.meta["causal"],
+                                  threads=self.threads)
         dt = time.perf_counter() - t0
-        one = dict(self.meta, B=1, H=len(sel))
+        one = dict(self.meta, B=1, H=n)
         return dt, decode_bytes(one)
 
     def heads_for_seconds(self, seconds):

@@ -63,3 +63,30 @@ def test_reference_arm_under_torchrun_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def _run_reference(extra):
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
+           "--impl", "reference", "--steps", "2", "--warmup", "1", "--ref-seconds", "1"] + extra
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    return json.loads(lines[0])
+
+
+def test_backward_reference_arm_under_torchrun_prints_once():
+    rec = _run_reference(["--op", "bwd", "--workload", "tiny"])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+    assert rec["metric"].startswith("attention bwd") and rec["unit"] == "TFLOP/s"
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_decode_reference_arm_under_torchrun_prints_once():
+    rec = _run_reference(["--op", "decode", "--workload", "decode_small"])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+    assert rec["metric"].startswith("decoding attention") and rec["unit"] == "GB/s"
+    assert rec["config"]["Nq"] == 2 and rec["config"]["Nk"] == 1024
