@@ -36,10 +36,12 @@ WORKLOADS = {
     # head dims outside the pages' 64 / 128 (the base shape otherwise)
     "hd32": (4, 32, 2048, 32, "fp16", (70, 71, 72)),
     "hd96": (4, 32, 2048, 96, "fp16", (73, 74, 75)),
+    # the base shape with a ragged length (2000 = 15 x 128 + 80)
+    "ragged": (4, 32, 2000, 64, "fp16", (76, 77, 78)),
 }
 # seed of the upstream gradient dO per workload (backward pass)
 DOUT_SEEDS = {"tiny": 3, "base": 13, "sweep_b1": 33, "sweep_b2": 34, "sweep_b4": 35,
-              "sweep_b8": 53, "d128": 36, "long": 44}
+              "sweep_b8": 53, "d128": 36, "long": 44, "hd32": 79, "hd96": 80, "ragged": 81}
 # seed of the query rows the oracle checks on the long-context workload
 LONG_ROW_SAMPLE_SEED = 43
 LONG_ROWS_PER_HEAD = 512

@@ -52,7 +52,7 @@ def test_head_dims_32_96_full(orc, dtype, d, causal, N):
     check_full(orc, q, k, v, d ** -0.5, causal, o, lse, "N=%d d=%d %s causal=%s" % (N, d, dtype, causal))
 
 
-@pytest.mark.parametrize("name", ["hd32", "hd96"])
+@pytest.mark.parametrize("name", ["hd32", "hd96", "ragged"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_head_dim_workloads_sampled(orc, name, causal):
     q, k, v, meta = inputs.make_workload(name)
