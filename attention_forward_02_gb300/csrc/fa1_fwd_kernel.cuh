@@ -35,7 +35,8 @@ constexpr uint32_t kCols = 512;      // S @ 0 (128), P V @ 128 (D), P @ 128 + D 
 
 template <int D>
 struct Cfg {
-    static constexpr int TILE = 128 * D * 2;
+    static_assert(D == 32 || D == 64 || D == 96 || D == 128, "head dims 32, 64, 96, 128");
+    static constexpr int TILE = 128 * col_blocks<D>() * 128;  // whole 128-byte swizzle blocks per row
     static constexpr int K_OFF = 0;                  // two stages
     static constexpr int V_OFF = K_OFF + 2 * TILE;   // two stages
     static constexpr int Q_OFF = V_OFF + 2 * TILE;   // two slots
@@ -121,11 +122,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j >= 2 && !(ok = wait_bounded(bar(C::B_KVEMPTY + s), ((j >> 1) - 1) & 1, abort_flag)))
                     break;
                 mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE);
-                for (int b = 0; b < D / 64; ++b)
+                for (int b = 0; b < col_blocks<D>(); ++b)
                     tma_load_3d(sbase + C::K_OFF + s * C::TILE + b * kSwAtomBytes, &tm_k,
                                 bar(C::B_KFULL + s), b * 64, j * kBlock, bh, pol);
                 mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE);
-                for (int b = 0; b < D / 64; ++b)
+                for (int b = 0; b < col_blocks<D>(); ++b)
                     tma_load_3d(sbase + C::V_OFF + s * C::TILE + b * kSwAtomBytes, &tm_v,
                                 bar(C::B_VFULL + s), b * 64, j * kBlock, bh, pol);
                 ++kv_issued;
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (t >= 2 && !(ok = wait_bounded(bar(C::B_QEMPTY + qs), ((t >> 1) - 1) & 1, abort_flag)))
                         break;
                     mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILE);
-                    for (int b = 0; b < D / 64; ++b)
+                    for (int b = 0; b < col_blocks<D>(); ++b)
                         tma_load_3d(sbase + C::Q_OFF + qs * C::TILE + b * kSwAtomBytes, &tm_q,
                                     bar(C::B_QFULL + qs), b * 64, i * kBlock, bh, pol);
                     ++q_issued;

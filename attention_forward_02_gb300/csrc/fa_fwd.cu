@@ -82,6 +82,14 @@ void init_device(int dev, DeviceState &st)
     if (e == cudaSuccess) e = set_smem_attr<64, true, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr<128, false, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr<128, true, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<32, false, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<32, true, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<96, false, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<96, true, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<32, false, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<32, true, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<96, false, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_fa1<96, true, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr_fa1<64, false, __half>();
     if (e == cudaSuccess) e = set_smem_attr_fa1<64, true, __half>();
     if (e == cudaSuccess) e = set_smem_attr_fa1<128, false, __half>();
@@ -124,6 +132,34 @@ fa_status_t launch_d(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
     FA_LAUNCH_D(96)
     FA_LAUNCH_D(128)
 #undef FA_LAUNCH_D
+    return FA_ERR_UNSUPPORTED;
+}
+
+template <int D, bool CAUSAL, typename T>
+fa_status_t launch_fa1(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
+                       float *lse, float *ws, int BH, int N, float scale, cudaStream_t stream);
+
+// Head-dim, causal and dtype dispatch of the FA1 launch.
+fa_status_t launch_fa1_any(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
+                           float *lse, float *ws, int BH, int N, int d, float scale, int causal, fa_dtype_t dtype,
+                           cudaStream_t stream)
+{
+#define FA1_D(DD, TT)                                                                                     \
+    if (d == DD)                                                                                          \
+        return causal ? launch_fa1<DD, true, TT>(mq, mk, mv, o, lse, ws, BH, N, scale, stream)            \
+                      : launch_fa1<DD, false, TT>(mq, mk, mv, o, lse, ws, BH, N, scale, stream);
+    if (dtype == FA_FP16) {
+        FA1_D(32, __half)
+        FA1_D(64, __half)
+        FA1_D(96, __half)
+        FA1_D(128, __half)
+    } else {
+        FA1_D(32, __nv_bfloat16)
+        FA1_D(64, __nv_bfloat16)
+        FA1_D(96, __nv_bfloat16)
+        FA1_D(128, __nv_bfloat16)
+    }
+#undef FA1_D
     return FA_ERR_UNSUPPORTED;
 }
 
@@ -310,7 +346,7 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
 
 size_t fa1_fwd_workspace_size(int B, int H, int N, int d)
 {
-    if (B < 0 || H < 0 || N < 0 || (d != 64 && d != 128))
+    if (B < 0 || H < 0 || N < 0 || (d != 32 && d != 64 && d != 96 && d != 128))
         return 0;
     return fa::fa1::workspace_floats(static_cast<long long>(B) * H, N, d) * sizeof(float);
 }
@@ -323,8 +359,6 @@ fa_status_t fa1_fwd(const void *q, const void *k, const void *v, void *o, float 
     fa_status_t s = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
     if (s != FA_OK || empty)
         return s;
-    if (d != 64 && d != 128)
-        return FA_ERR_UNSUPPORTED;  // the FA1 baseline is built for the pages' head dims
     const size_t need = fa1_fwd_workspace_size(B, H, N, d);
     if (!workspace || workspace_bytes < need)
         return FA_ERR_INVALID_ARG;
@@ -345,18 +379,7 @@ fa_status_t fa1_fwd(const void *q, const void *k, const void *v, void *o, float 
         return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     float *ws = static_cast<float *>(workspace);
-    if (dtype == FA_FP16) {
-        if (d == 64)
-            return causal ? launch_fa1<64, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
-                          : launch_fa1<64, false, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
-        return causal ? launch_fa1<128, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
-                      : launch_fa1<128, false, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
-    }
-    if (d == 64)
-        return causal ? launch_fa1<64, true, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
-                      : launch_fa1<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
-    return causal ? launch_fa1<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
-                  : launch_fa1<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+    return launch_fa1_any(mq, mk, mv, o, lse, ws, bh, N, d, scale, causal, dtype, cs);
 }
 
 fa_status_t fa1_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -367,8 +390,6 @@ fa_status_t fa1_fwd_noalloc(const void *q, const void *k, const void *v, void *o
     fa_status_t s = check_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &empty);
     if (s != FA_OK || empty)
         return s;
-    if (d != 64 && d != 128)
-        return FA_ERR_UNSUPPORTED;
     if (fa1_fwd_workspace_size(B, H, N, d) > kNoAllocScratchBytes)
         return FA_ERR_UNSUPPORTED;  // problem needs more scratch than the fixed array holds
     int dev = -1;
@@ -384,18 +405,7 @@ fa_status_t fa1_fwd_noalloc(const void *q, const void *k, const void *v, void *o
         return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     float *ws = na.scratch;
-    if (dtype == FA_FP16) {
-        if (d == 64)
-            return causal ? launch_fa1<64, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
-                          : launch_fa1<64, false, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
-        return causal ? launch_fa1<128, true, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
-                      : launch_fa1<128, false, __half>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
-    }
-    if (d == 64)
-        return causal ? launch_fa1<64, true, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
-                      : launch_fa1<64, false, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
-    return causal ? launch_fa1<128, true, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs)
-                  : launch_fa1<128, false, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, N, scale, cs);
+    return launch_fa1_any(mq, mk, mv, o, lse, ws, bh, N, d, scale, causal, dtype, cs);
 }
 
 fa_status_t fa_last_device_status(void *stream)

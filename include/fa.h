@@ -73,7 +73,7 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
  *  B, H, N : batch, heads, sequence length (queries = keys = N).  Any of them
  *            0 is an empty problem: FA_OK, nothing launched.  Ragged N (not a
  *            multiple of the 128-row tile) is supported.
- *  d       : head dimension, 32, 64, 96 or 128 (fa1_fwd: 64 or 128).
+ *  d       : head dimension, 32, 64, 96 or 128.
  *  scale   : score scale (1/sqrt(d) for standard attention); finite, >= 0.
  *  causal  : 0 = every key; 1 = query i attends to keys j <= i.
  *  dtype   : FA_FP16 or FA_BF16.

@@ -77,7 +77,8 @@ def test_argument_checks(lib, kwargs, status):
 def test_fa1_workspace_size(lib):
     assert fa.fa1_fwd_workspace_size(4, 32, 2048, 64) == 4 * 32 * 2048 * 66 * 4
     assert fa.fa1_fwd_workspace_size(1, 1, 1, 128) == 130 * 4
-    assert fa.fa1_fwd_workspace_size(1, 1, 1, 96) == 0
+    assert fa.fa1_fwd_workspace_size(1, 1, 1, 96) == 98 * 4
+    assert fa.fa1_fwd_workspace_size(1, 1, 1, 48) == 0
     assert fa.fa1_fwd_workspace_size(-1, 1, 1, 64) == 0
 
 
@@ -93,7 +94,7 @@ def call_fa1(ws=W, ws_bytes=1 << 30, **kw):
 
 @pytest.mark.parametrize("kwargs,status", [
     (dict(ws=0), 1), (dict(ws_bytes=100), 1), (dict(ws=W + 8), 3), (dict(ws=Q), 1),
-    (dict(d=96), 2), (dict(d=32), 2), (dict(causal=3), 1), (dict(N=0), 0),
+    (dict(d=48), 2), (dict(causal=3), 1), (dict(N=0), 0),
 ], ids=lambda x: str(x))
 def test_fa1_argument_checks(lib, kwargs, status):
     assert call_fa1(**kwargs) == status

@@ -43,6 +43,16 @@ def test_ragged_full(orc, dtype, d, causal, N):
     check_full(orc, q, k, v, d ** -0.5, causal, o, lse, "fa1 N=%d d=%d %s causal=%s" % (N, d, dtype, causal))
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("d", [32, 96])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 129, 640])
+def test_head_dims_32_96_full(orc, dtype, d, causal, N):
+    q, k, v = inputs.make_qkv(1, 2, N, d, dtype, (4100 + N + d, 5100 + N, 6100 + d))
+    o, lse = run_fa1(q, k, v, d ** -0.5, causal)
+    check_full(orc, q, k, v, d ** -0.5, causal, o, lse, "fa1 N=%d d=%d %s causal=%s" % (N, d, dtype, causal))
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_stress_full(orc, causal):
     q, k, v = inputs.make_qkv(1, 4, 1024, 64, "fp16", (71, 72, 73), q_scale=8.0)
