@@ -515,29 +515,78 @@ def main():
         dist.destroy_process_group()
 
 
+def pipelined_e2e(torch, dev, steps, h2d, compute, d2h):
+    """Runs `steps` end-to-end steps with the host->device copies of step i+1
+    and the device->host copies of step i-1 overlapping the compute of step
+    i: three streams, two device buffer sets, events for every dependency.
+    h2d(b, stream), compute(b, stream), d2h(b, stream) enqueue one step's
+    copies / kernels for buffer set b.  Every step moves all its bytes; the
+    time runs from the first copy in to the last copy out.  Returns ms."""
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    start.record(s_in)
+    for i in range(steps):
+        b = i & 1
+        if i >= 2:
+            s_in.wait_event(comp_done[b])  # step i-2 has finished reading buffer set b
+        h2d(b, s_in)
+        in_done[b].record(s_in)
+        s_comp.wait_event(in_done[b])
+        if i >= 2:
+            s_comp.wait_event(out_done[b])  # step i-2's results have been copied out
+        compute(b, s_comp)
+        comp_done[b].record(s_comp)
+        s_out.wait_event(comp_done[b])
+        d2h(b, s_out)
+        out_done[b].record(s_out)
+    end.record(s_out)
+    torch.cuda.synchronize(dev)
+    return start.elapsed_time(end)
+
+
 def run_e2e(run, torch, q, k, v, meta, variants, dev, stream, scale, step_flops, steps, dist):
+    """End to end through the public API from pinned host buffers: per step
+    the H2D copy of q, k, v, every variant's launch, and the D2H copy of every
+    variant's O and LSE.  Reported value: the pipelined run (copies of the
+    neighbouring steps overlap this step's kernels); `serial` is the same
+    steps one after another on one stream."""
     hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    qd, kd, vd = torch.empty_like(hq, device=dev), torch.empty_like(hk, device=dev), \
-        torch.empty_like(hv, device=dev)
-    houts = [(torch.empty_like(hq).pin_memory(),
-              torch.empty((meta["B"], meta["H"], meta["N"]), dtype=torch.float32).pin_memory())
+    B, H, N = meta["B"], meta["H"], meta["N"]
+    houts = [(torch.empty_like(hq).pin_memory(), torch.empty((B, H, N), dtype=torch.float32).pin_memory())
              for _ in variants]
-    douts = [(torch.empty_like(qd), torch.empty((meta["B"], meta["H"], meta["N"]),
-                                                dtype=torch.float32, device=dev)) for _ in variants]
+    dins = [tuple(torch.empty_like(hq, device=dev) for _ in range(3)) for _ in range(2)]
+    douts = [[(torch.empty_like(hq, device=dev), torch.empty((B, H, N), dtype=torch.float32, device=dev))
+              for _ in variants] for _ in range(2)]
     h2d = 3 * hq.numel() * hq.element_size()
     d2h = sum(o.numel() * o.element_size() + l.numel() * 4 for o, l in houts)
 
-    def one():
-        qd.copy_(hq, non_blocking=True)
-        kd.copy_(hk, non_blocking=True)
-        vd.copy_(hv, non_blocking=True)
-        for (o, l), (ho, hl), causal in zip(douts, houts, variants):
-            run(qd, kd, vd, o=o, lse=l, scale=scale, causal=causal, stream=stream)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(l, non_blocking=True)
+    def copy_in(b, st):
+        with torch.cuda.stream(st):
+            for dst, src in zip(dins[b], (hq, hk, hv)):
+                dst.copy_(src, non_blocking=True)
+
+    def compute(b, st):
+        qd, kd, vd = dins[b]
+        for (o, l), causal in zip(douts[b], variants):
+            run(qd, kd, vd, o=o, lse=l, scale=scale, causal=causal, stream=st)
+
+    def copy_out(b, st):
+        with torch.cuda.stream(st):
+            for (o, l), (ho, hl) in zip(douts[b], houts):
+                ho.copy_(o, non_blocking=True)
+                hl.copy_(l, non_blocking=True)
+
+    def serial_step():
+        copy_in(0, stream)
+        compute(0, stream)
+        copy_out(0, stream)
 
     for _ in range(3):
-        one()
+        serial_step()
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
@@ -545,17 +594,24 @@ def run_e2e(run, torch, q, k, v, meta, variants, dev, stream, scale, step_flops,
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(steps):
-        one()
+        serial_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
+    ms_serial = e0.elapsed_time(e1)
+    pipelined_e2e(torch, dev, 3, copy_in, compute, copy_out)  # warm-up of the streams
+    if dist is not None:
+        dist.barrier()
+    ms = pipelined_e2e(torch, dev, steps, copy_in, compute, copy_out)
+    flops = step_flops * steps
     if dist is not None:
         ms = max_over_ranks(dist, ms, dev)
-        flops = sum_over_ranks(dist, step_flops * steps, dev)
-    else:
-        flops = step_flops * steps
+        ms_serial = max_over_ranks(dist, ms_serial, dev)
+        flops = sum_over_ranks(dist, flops, dev)
     return {"value": flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+            "mode": "pipelined: step i+1's H2D and step i-1's D2H overlap step i's kernels "
+                    "(3 streams, 2 device buffer sets)",
+            "serial": {"value": flops / (ms_serial / 1e3) / 1e12, "ms_per_step": ms_serial / steps}}
 
 
 def run_reference(args, q, k, v, meta, variants, config, step_flops, world, rank):
@@ -699,56 +755,74 @@ def run_bwd(args, q, k, v, do, meta, variants, config, world, rank, local):
 
 
 def run_e2e_bwd(fa, torch, q, k, v, do, meta, variants, dev, stream, scale, step_flops, steps, dist):
-    """Backward through the public API from pinned host buffers: per step the
-    H2D copy of q, k, v, o, lse, dO (o, lse made once by the forward), the
-    backward, and the D2H copy of dq, dk, dv, for each variant."""
+    """Backward through the public API from pinned host buffers: per step and
+    variant the H2D copy of q, k, v, o, lse, dO (o, lse made once by the
+    forward), the backward, and the D2H copy of dq, dk, dv.  Pipelined as the
+    forward's e2e; `serial` is the same steps on one stream."""
     B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
     hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
-    dq_, dk_, dv_, ddo = (torch.empty_like(hq, device=dev) for _ in range(4))
-    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     host_fwd = []
     for c in variants:
         o, l = fa.fa_fwd(hq.to(dev), hk.to(dev), hv.to(dev), scale=scale, causal=c)
         host_fwd.append((o.cpu().pin_memory(), l.cpu().pin_memory()))
-    od = torch.empty_like(dq_)
-    ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     outs_h = [tuple(torch.empty_like(hq).pin_memory() for _ in range(3)) for _ in variants]
-    grads_d = tuple(torch.empty_like(dq_) for _ in range(3))
-    h2d = len(variants) * (5 * hq.numel() * hq.element_size() + ld.numel() * 4)
+    # per buffer set and variant: q, k, v, dO, o (16-bit) + lse; grads; a workspace
+    dins = [[(tuple(torch.empty_like(hq, device=dev) for _ in range(5)),
+              torch.empty((B, H, N), dtype=torch.float32, device=dev)) for _ in variants] for _ in range(2)]
+    dgrads = [[tuple(torch.empty_like(hq, device=dev) for _ in range(3)) for _ in variants] for _ in range(2)]
+    wss = [torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev) for _ in range(2)]
+    h2d = len(variants) * (5 * hq.numel() * hq.element_size() + B * H * N * 4)
     d2h = len(variants) * 3 * hq.numel() * hq.element_size()
 
-    def one():
-        for (ho, hl), (hdq, hdk, hdv), c in zip(host_fwd, outs_h, variants):
-            dq_.copy_(hq, non_blocking=True)
-            dk_.copy_(hk, non_blocking=True)
-            dv_.copy_(hv, non_blocking=True)
-            ddo.copy_(hdo, non_blocking=True)
-            od.copy_(ho, non_blocking=True)
-            ld.copy_(hl, non_blocking=True)
-            fa.fa_bwd(dq_, dk_, dv_, od, ld, ddo, scale=scale, causal=c, dq=grads_d[0],
-                      dk=grads_d[1], dv=grads_d[2], workspace=ws, stream=stream)
-            hdq.copy_(grads_d[0], non_blocking=True)
-            hdk.copy_(grads_d[1], non_blocking=True)
-            hdv.copy_(grads_d[2], non_blocking=True)
+    def copy_in(b, st):
+        with torch.cuda.stream(st):
+            for ((t16, ld), (ho, hl)) in zip(dins[b], host_fwd):
+                for dst, src in zip(t16, (hq, hk, hv, hdo, ho)):
+                    dst.copy_(src, non_blocking=True)
+                ld.copy_(hl, non_blocking=True)
+
+    def compute(b, st):
+        for ((qd, kd, vd, dod, od), ld), g, c in zip(dins[b], dgrads[b], variants):
+            fa.fa_bwd(qd, kd, vd, od, ld, dod, scale=scale, causal=c, dq=g[0], dk=g[1], dv=g[2],
+                      workspace=wss[b], stream=st)
+
+    def copy_out(b, st):
+        with torch.cuda.stream(st):
+            for g, hg in zip(dgrads[b], outs_h):
+                for src, dst in zip(g, hg):
+                    dst.copy_(src, non_blocking=True)
+
+    def serial_step():
+        copy_in(0, stream)
+        compute(0, stream)
+        copy_out(0, stream)
 
     for _ in range(3):
-        one()
+        serial_step()
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(steps):
-        one()
+        serial_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
+    ms_serial = e0.elapsed_time(e1)
+    pipelined_e2e(torch, dev, 3, copy_in, compute, copy_out)
+    if dist is not None:
+        dist.barrier()
+    ms = pipelined_e2e(torch, dev, steps, copy_in, compute, copy_out)
     flops = step_flops * steps
     if dist is not None:
         ms = max_over_ranks(dist, ms, dev)
+        ms_serial = max_over_ranks(dist, ms_serial, dev)
         flops = sum_over_ranks(dist, flops, dev)
     return {"value": flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+            "mode": "pipelined: step i+1's H2D and step i-1's D2H overlap step i's kernels "
+                    "(3 streams, 2 device buffer sets)",
+            "serial": {"value": flops / (ms_serial / 1e3) / 1e12, "ms_per_step": ms_serial / steps}}
 
 
 def run_reference_bwd(args, q, k, v, do, meta, variants, config, world, rank):
