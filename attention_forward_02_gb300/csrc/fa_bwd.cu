@@ -72,7 +72,7 @@ struct Maps {
 
 template <int D, bool CAUSAL, typename T>
 fa_status_t launch(const Maps &mp, const void *o, const float *lse, const void *dout, void *dq, float *acc,
-                   float *lse2, float *dvec, int BH, int N, float scale, cudaStream_t stream)
+                   float *lse2, float *dvec, int BH, int N, float scale, int num_sms, cudaStream_t stream)
 {
     using namespace fa::bwd;
     const long long Npad = padded_rows(N);
@@ -86,7 +86,11 @@ fa_status_t launch(const Maps &mp, const void *o, const float *lse, const void *
                                                             acc, N, static_cast<int>(Npad), rows);
     }
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    fa_bwd_kernel<D, CAUSAL, T><<<static_cast<unsigned>(BH * nb), kThreads, Cfg<D>::SMEM_ALLOC, stream>>>(
+    // persistent: one CTA per SM (shared memory and TMEM allow no more), each
+    // walking its share of the BH * nb (head, key block) items
+    const long long items = static_cast<long long>(BH) * nb;
+    const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
+    fa_bwd_kernel<D, CAUSAL, T><<<grid, kThreads, Cfg<D>::SMEM_ALLOC, stream>>>(
         mp.q, mp.k, mp.v, mp.dout, mp.dk, mp.dv, mp.acc, lse2, dvec, N, static_cast<int>(Npad), BH, nb, scale,
         scale_log2);
     {
@@ -148,8 +152,8 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
         return FA_ERR_INVALID_ARG;
     const long long BH = static_cast<long long>(B) * H;
     const long long Npad = padded_rows(N);
-    if (BH * (Npad / fa::bwd::kBlk) > 0x7fffffffLL)
-        return FA_ERR_UNSUPPORTED;  // grid.x limit
+    if (BH * (Npad / fa::bwd::kBlk) > 0x7fffffffLL - 65536)
+        return FA_ERR_UNSUPPORTED;  // item numbers (plus one round of CTAs) are 32-bit
     const size_t bytes = static_cast<size_t>(BH) * N * d * 2;
     const size_t lbytes = static_cast<size_t>(BH) * N * sizeof(float);
     const uintptr_t outs[4] = {reinterpret_cast<uintptr_t>(dq), reinterpret_cast<uintptr_t>(dk),
@@ -169,8 +173,11 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     }
 
     EncodeTiledFn encode = nullptr;
-    if ((s = fa_host::encoder(&encode, nullptr)) != FA_OK)
+    int num_sms = 0;
+    if ((s = fa_host::encoder(&encode, &num_sms)) != FA_OK)
         return s;
+    if (num_sms < 1)
+        return FA_ERR_CUDA;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return FA_ERR_CUDA;
@@ -193,7 +200,7 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     if ((s = encode_acc_map(encode, &mp.acc, acc, bh, Npad, d)) != FA_OK) return s;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-#define FA_BWD_ARGS mp, o, lse, dout, dq, acc, lse2, dvec, bh, N, scale, cs
+#define FA_BWD_ARGS mp, o, lse, dout, dq, acc, lse2, dvec, bh, N, scale, num_sms, cs
 #define FA_BWD_D(DD, TT)                                                                                  \
     if (d == DD)                                                                                          \
         return causal ? launch<DD, true, TT>(FA_BWD_ARGS) : launch<DD, false, TT>(FA_BWD_ARGS);

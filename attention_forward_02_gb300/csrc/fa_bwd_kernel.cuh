@@ -14,10 +14,13 @@
 // Three launches:
 //   fa_bwd_prep_kernel  D_i and L_i * log2(e) into a padded per-head layout,
 //                       and zeroes the fp32 dQ accumulator.
-//   fa_bwd_kernel       one CTA per (batch*head, 128-key block): K_n and V_n
-//                       stay in shared memory; the CTA walks the query blocks
-//                       m (all of them, or m >= n when causal) and keeps dK_n
-//                       and dV_n in TMEM for the whole walk.  Per query block:
+//   fa_bwd_kernel       persistent, one CTA per SM; a work item is one
+//                       (batch*head, 128-key block n): K_n and V_n stay in
+//                       shared memory while the CTA walks the query blocks m
+//                       (all of them, or m >= n when causal) and keeps dK_n
+//                       and dV_n in TMEM for the whole walk.  The next item's
+//                       K, V and first Q, dO loads overlap the epilogue that
+//                       writes dK_n and dV_n.  Per query block:
 //                         S^T  = K_n Q_m^T           (tcgen05, TMEM)
 //                         dP^T = V_n dO_m^T          (tcgen05, TMEM)
 //                         P^T  = 2^(S^T scale log2e - L_m log2e)   (warps 0-7)
@@ -121,7 +124,8 @@ struct Cfg {
     static constexpr int DD_OFF = L_OFF + QST * kBlk * 4;      // DOST x 128 fp32
     static constexpr int BAR_OFF = DD_OFF + DOST * kBlk * 4;
     static constexpr int B_KVFULL = 0;
-    static constexpr int B_QFULL = 1;
+    static constexpr int B_KVEMPTY = 1;
+    static constexpr int B_QFULL = 2;
     static constexpr int B_QEMPTY = B_QFULL + QST;
     static constexpr int B_DOFULL = B_QEMPTY + QST;
     static constexpr int B_DOEMPTY = B_DOFULL + DOST;
@@ -141,9 +145,10 @@ struct Cfg {
     static_assert(DS_OFF % 1024 == 0 && STG_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 };
 
-// Work item of CTA w: (head bh, key block n).  Causal: the heaviest key blocks
-// (low n, which see the most query blocks) of every head first.  Non-causal:
-// head-major, so CTAs running together share one head's Q and dO in L2.
+// Work item number w: (head bh, key block n).  Causal: the heaviest key
+// blocks (low n, which see the most query blocks) of every head first.
+// Non-causal: head-major, so CTAs running together share one head's Q and dO
+// in L2.
 template <bool CAUSAL>
 __device__ __forceinline__ void item_coords(int w, int BH, int nb, int &bh, int &n)
 {
@@ -154,6 +159,23 @@ __device__ __forceinline__ void item_coords(int w, int BH, int nb, int &bh, int 
         bh = w / nb;
         n = w % nb;
     }
+}
+
+// Item k of this CTA (the kernel is persistent: gridDim.x CTAs, at most one
+// per SM).  Round k deals items [k G, k G + G) out to the G CTAs, every other
+// round in reverse CTA order, so that the heavy and light causal items of
+// consecutive rounds even out per CTA.  False past the last item.
+template <bool CAUSAL>
+__device__ __forceinline__ bool item_of(int k, int BH, int nb, int &bh, int &n)
+{
+    // (the host keeps BH * nb + gridDim.x within int range)
+    const int G = static_cast<int>(gridDim.x);
+    const int cta = static_cast<int>(blockIdx.x);
+    const int w = k * G + ((k & 1) ? G - 1 - cta : cta);
+    if (w >= BH * nb)
+        return false;
+    item_coords<CAUSAL>(w, BH, nb, bh, n);
+    return true;
 }
 
 template <int D, bool CAUSAL, typename T>
@@ -177,10 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    int bh, n;
-    item_coords<CAUSAL>(static_cast<int>(blockIdx.x), BH, nb, bh, n);
-    const int m0 = CAUSAL ? n : 0;  // first query block that sees key block n
-    const int cnt = nb - m0;        // query blocks walked (>= 1)
+    // Every role walks the same item sequence; g counts the query blocks of
+    // all earlier items (the ring slots and barrier phases run on across items).
+    int bh = 0, n = 0;
 
     auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + C::SLOT_OFF);
@@ -188,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_KVFULL), 1);
+        mbar_init(bar(C::B_KVEMPTY), 1);
         for (int s = 0; s < QST; ++s) {
             mbar_init(bar(C::B_QFULL + s), 1);
             mbar_init(bar(C::B_QEMPTY + s), 1);
@@ -227,39 +249,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             // of the head.
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
-            for (int b = 0; b < col_blocks<D>(); ++b) {
-                tma_load_3d(sbase + C::K_OFF + b * kSwAtomBytes, &tm_k, bar(C::B_KVFULL), b * 64, n * kBlk,
-                            bh, pol_kv);
-                tma_load_3d(sbase + C::V_OFF + b * kSwAtomBytes, &tm_v, bar(C::B_KVFULL), b * 64, n * kBlk,
-                            bh, pol_kv);
-            }
-            int nq = 0, ndo = 0;
-            bool ok = true;
-            for (int i = 0; ok && i < cnt; ++i) {
-                const int m = m0 + i;
+            int nq = 0, ndo = 0, nkv = 0;
+            // Q_m (+ L_m) and dO_m (+ D_m) of global query block nq into their ring slots
+            auto load_block = [&](int m) -> bool {
                 const size_t row0 = static_cast<size_t>(bh) * Npad + static_cast<size_t>(m) * kBlk;
-                const int s = i % QST;
-                if (i >= QST && !(ok = wait_bounded(bar(C::B_QEMPTY + s), ((i / QST) - 1) & 1, abort_flag)))
-                    break;
+                const int s = nq % QST;
+                if (nq >= QST && !wait_bounded(bar(C::B_QEMPTY + s), ((nq / QST) - 1) & 1, abort_flag))
+                    return false;
                 mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE + kBlk * 4);
                 for (int b = 0; b < col_blocks<D>(); ++b)
                     tma_load_3d(sbase + C::Q_OFF + s * C::TILE + b * kSwAtomBytes, &tm_q, bar(C::B_QFULL + s),
                                 b * 64, m * kBlk, bh, pol_q);
                 bulk_load(sbase + C::L_OFF + s * kBlk * 4, lse2 + row0, kBlk * 4, bar(C::B_QFULL + s));
                 ++nq;
-                const int ds = i % DOST;
-                if (i >= DOST && !(ok = wait_bounded(bar(C::B_DOEMPTY + ds), ((i / DOST) - 1) & 1, abort_flag)))
-                    break;
+                const int ds = ndo % DOST;
+                if (ndo >= DOST && !wait_bounded(bar(C::B_DOEMPTY + ds), ((ndo / DOST) - 1) & 1, abort_flag))
+                    return false;
                 mbar_arrive_expect_tx(bar(C::B_DOFULL + ds), C::TILE + kBlk * 4);
                 for (int b = 0; b < col_blocks<D>(); ++b)
                     tma_load_3d(sbase + C::DO_OFF + ds * C::TILE + b * kSwAtomBytes, &tm_do,
                                 bar(C::B_DOFULL + ds), b * 64, m * kBlk, bh, pol_q);
                 bulk_load(sbase + C::DD_OFF + ds * kBlk * 4, dvec + row0, kBlk * 4, bar(C::B_DOFULL + ds));
                 ++ndo;
+                return true;
+            };
+            bool ok = true;
+            for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, bh, n); ++k) {
+                const int m0 = CAUSAL ? n : 0;  // first query block that sees key block n
+                const int cnt = nb - m0;        // query blocks walked (>= 1)
+                // the first query block ahead of K_n, V_n: its ring slots free up
+                // before the previous item's last products have read K and V
+                if (!(ok = load_block(m0)))
+                    break;
+                if (k > 0 && !(ok = wait_bounded(bar(C::B_KVEMPTY), (k - 1) & 1, abort_flag)))
+                    break;
+                mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
+                for (int b = 0; b < col_blocks<D>(); ++b) {
+                    tma_load_3d(sbase + C::K_OFF + b * kSwAtomBytes, &tm_k, bar(C::B_KVFULL), b * 64, n * kBlk,
+                                bh, pol_kv);
+                    tma_load_3d(sbase + C::V_OFF + b * kSwAtomBytes, &tm_v, bar(C::B_KVFULL), b * 64, n * kBlk,
+                                bh, pol_kv);
+                }
+                ++nkv;
+                for (int i = 1; ok && i < cnt; ++i)
+                    ok = load_block(m0 + i);
             }
             // wait for every copy this thread issued
-            drain_bounded(bar(C::B_KVFULL), 0);
+            if (nkv > 0)
+                drain_bounded(bar(C::B_KVFULL), (nkv - 1) & 1);
             for (int s = 0; s < QST; ++s)
                 if (nq > s)
                     drain_bounded(bar(C::B_QFULL + s), ((nq - 1 - s) / QST) & 1);
@@ -323,74 +360,90 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_f16_ss(tmem + col_dq<D>(), ds_mn + mn(kk), k_mn + mn(kk), idesc_dq, kk > 0 ? 1u : 0u);
             };
 
-            bool ok = wait_bounded(bar(C::B_KVFULL), 0, abort_flag) &&
-                      wait_bounded(bar(C::B_QFULL), 0, abort_flag);
-            if (ok) {
+            bool ok = true;
+            int g = 0;
+            for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, bh, n); ++k) {
+                const int cnt = nb - (CAUSAL ? n : 0);
+                // S^T of the item's first block: the previous item's last dV
+                // product, issued earlier, has read P^T from these columns
+                if (!(ok = wait_bounded(bar(C::B_KVFULL), k & 1, abort_flag) &&
+                           wait_bounded(bar(C::B_QFULL + g % QST), (g / QST) & 1, abort_flag)))
+                    break;
                 tc_fence_after();
-                issue_s(0);
+                issue_s(g % QST);
                 umma_commit(bar(C::B_SFULL));
-                ok = wait_bounded(bar(C::B_DOFULL), 0, abort_flag);
-            }
-            if (ok) {
+                // D > 64: the previous block's dQ sits in the dP^T columns until
+                // warps 8-11 have read it out
+                if (!(ok = (!C::DQ_ALIAS || g == 0 || wait_bounded(bar(C::B_DQFREE), (g - 1) & 1, abort_flag)) &&
+                           wait_bounded(bar(C::B_DOFULL + g % DOST), (g / DOST) & 1, abort_flag)))
+                    break;
                 tc_fence_after();
-                issue_dp(0);
+                issue_dp(g % DOST);
                 umma_commit(bar(C::B_DPFULL));
-            }
-            for (int i = 0; ok && i < cnt; ++i) {
-                const int s = i % QST, ds = i % DOST;
-                const uint32_t ph = static_cast<uint32_t>(i & 1);
-                if (!(ok = wait_bounded(bar(C::B_PFULL), ph, abort_flag)))
+                for (int i = 0; ok && i < cnt; ++i) {
+                    const int gi = g + i;
+                    const int s = gi % QST, ds = gi % DOST;
+                    const uint32_t ph = static_cast<uint32_t>(gi & 1);
+                    // (block 0: the compute warps arrive here after reading the
+                    // previous item's dV and dK out of TMEM, so they may be reset)
+                    if (!(ok = wait_bounded(bar(C::B_PFULL), ph, abort_flag)))
+                        break;
+                    tc_fence_after();
+                    issue_dv(ds, i > 0);
+                    if (i + 1 < cnt) {
+                        // S^T of the next block overwrites P^T, after the dV product
+                        // above has read it (one thread's MMAs run in issue order)
+                        const int s1 = (gi + 1) % QST;
+                        if (!(ok = wait_bounded(bar(C::B_QFULL + s1), ((gi + 1) / QST) & 1, abort_flag)))
+                            break;
+                        tc_fence_after();
+                        issue_s(s1);
+                        umma_commit(bar(C::B_SFULL));
+                    }
+                    if (!(ok = wait_bounded(bar(C::B_DSFULL), ph, abort_flag)))
+                        break;
+                    tc_fence_after();
+                    // the compute warps are done with D_m; dP^T and dV have read dO_m
+                    umma_commit(bar(C::B_DOEMPTY + ds));
+                    const int ds1 = (gi + 1) % DOST;
+                    if (!C::DQ_ALIAS && i + 1 < cnt) {
+                        // D <= 64: dP^T of the next block first (its columns are
+                        // free: dS^T has columns of its own), so the compute warps
+                        // can go on
+                        if (!(ok = wait_bounded(bar(C::B_DOFULL + ds1), ((gi + 1) / DOST) & 1, abort_flag)))
+                            break;
+                        tc_fence_after();
+                        issue_dp(ds1);
+                        umma_commit(bar(C::B_DPFULL));
+                    }
+                    // D > 64: dK reads dS^T from the dP^T columns before dQ writes
+                    // them (one thread's MMAs run in issue order)
+                    issue_dk(s, i > 0);
+                    if (!C::DQ_ALIAS && gi > 0) {
+                        if (!(ok = wait_bounded(bar(C::B_DQFREE), (gi - 1) & 1, abort_flag)))
+                            break;
+                        tc_fence_after();
+                    }
+                    issue_dq();
+                    umma_commit(bar(C::B_DQFULL));
+                    umma_commit(bar(C::B_QEMPTY + s));
+                    if (C::DQ_ALIAS && i + 1 < cnt) {
+                        // dQ_m sits in the dP^T columns: wait until it is read out
+                        if (!(ok = wait_bounded(bar(C::B_DQFREE), ph, abort_flag) &&
+                                   wait_bounded(bar(C::B_DOFULL + ds1), ((gi + 1) / DOST) & 1, abort_flag)))
+                            break;
+                        tc_fence_after();
+                        issue_dp(ds1);
+                        umma_commit(bar(C::B_DPFULL));
+                    }
+                }
+                if (!ok)
                     break;
-                tc_fence_after();
-                issue_dv(ds, i > 0);
-                if (i + 1 < cnt) {
-                    // S^T of the next block overwrites P^T, after the dV product
-                    // above has read it (one thread's MMAs run in issue order)
-                    const int s1 = (i + 1) % QST;
-                    if (!(ok = wait_bounded(bar(C::B_QFULL + s1), ((i + 1) / QST) & 1, abort_flag)))
-                        break;
-                    tc_fence_after();
-                    issue_s(s1);
-                    umma_commit(bar(C::B_SFULL));
-                }
-                if (!(ok = wait_bounded(bar(C::B_DSFULL), ph, abort_flag)))
-                    break;
-                tc_fence_after();
-                // the compute warps are done with D_m; dP^T and dV have read dO_m
-                umma_commit(bar(C::B_DOEMPTY + ds));
-                const int ds1 = (i + 1) % DOST;
-                if (!C::DQ_ALIAS && i + 1 < cnt) {
-                    // D = 64: dP^T of the next block first (its columns are free:
-                    // dS^T has columns of its own), so the compute warps can go on
-                    if (!(ok = wait_bounded(bar(C::B_DOFULL + ds1), ((i + 1) / DOST) & 1, abort_flag)))
-                        break;
-                    tc_fence_after();
-                    issue_dp(ds1);
-                    umma_commit(bar(C::B_DPFULL));
-                }
-                // D = 128: dK reads dS^T from the dP^T columns before dQ writes
-                // them (one thread's MMAs run in issue order)
-                issue_dk(s, i > 0);
-                if (!C::DQ_ALIAS && i > 0) {
-                    if (!(ok = wait_bounded(bar(C::B_DQFREE), (i - 1) & 1, abort_flag)))
-                        break;
-                    tc_fence_after();
-                }
-                issue_dq();
-                umma_commit(bar(C::B_DQFULL));
-                umma_commit(bar(C::B_QEMPTY + s));
-                if (C::DQ_ALIAS && i + 1 < cnt) {
-                    // dQ_m sits in the dP^T columns: wait until it is read out
-                    if (!(ok = wait_bounded(bar(C::B_DQFREE), ph, abort_flag) &&
-                               wait_bounded(bar(C::B_DOFULL + ds1), ((i + 1) / DOST) & 1, abort_flag)))
-                        break;
-                    tc_fence_after();
-                    issue_dp(ds1);
-                    umma_commit(bar(C::B_DPFULL));
-                }
-            }
-            if (ok)
+                // dK_n, dV_n are final; K_n, V_n are no longer read
                 umma_commit(bar(C::B_DKVFULL));
+                umma_commit(bar(C::B_KVEMPTY));
+                g += cnt;
+            }
             // every MMA this thread issued has completed once this arrives
             umma_commit(bar(C::B_DRAIN));
             drain_bounded(bar(C::B_DRAIN), 0);
@@ -401,40 +454,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t dq_tm = tmem + lane_base + col_dq<D>();
         const bool leader = threadIdx.x == kDqWarp0 * 32;
-        int chunk = 0;
-        for (int i = 0; i < cnt; ++i) {
-            bool ok = wait_bounded(bar(C::B_DQFULL), static_cast<uint32_t>(i & 1), abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (named_bar_or(3, 128, !ok))
-                break;
-            tc_fence_after();
-            const int m = m0 + i;
-#pragma unroll 1
-            for (int c4 = 0; c4 < D / 32; ++c4, ++chunk) {
-                uint32_t u[32];
-                tmem_ld32(dq_tm + 32 * c4, u);
-                if (c4 == D / 32 - 1) {
-                    // dQ_m has been read out: its TMEM columns are free
-                    tc_fence_before();
-                    mbar_arrive(bar(C::B_DQFREE));
+        int chunk = 0, g = 0;
+        bool ok = true;
+        for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, bh, n); ++k) {
+            const int m0 = CAUSAL ? n : 0;
+            const int cnt = nb - m0;
+            for (int i = 0; i < cnt; ++i) {
+                bool w = wait_bounded(bar(C::B_DQFULL), static_cast<uint32_t>((g + i) & 1), abort_flag);
+                w = __all_sync(0xffffffffu, w);
+                if (named_bar_or(3, 128, !w)) {
+                    ok = false;
+                    break;
                 }
-                const int stg = chunk % NSTG;
-                const uint32_t sbuf = sbase + C::STG_OFF + stg * C::STG_BYTES;
-                // the reduce that last read this staging buffer has finished reading
-                if (leader && chunk >= NSTG)
-                    bulk_wait_group_read<NSTG - 1>();
-                named_bar_sync(3, 128);
+                tc_fence_after();
+                const int m = m0 + i;
+#pragma unroll 1
+                for (int c4 = 0; c4 < D / 32; ++c4, ++chunk) {
+                    uint32_t u[32];
+                    tmem_ld32(dq_tm + 32 * c4, u);
+                    if (c4 == D / 32 - 1) {
+                        // dQ_m has been read out: its TMEM columns are free
+                        tc_fence_before();
+                        mbar_arrive(bar(C::B_DQFREE));
+                    }
+                    const int stg = chunk % NSTG;
+                    const uint32_t sbuf = sbase + C::STG_OFF + stg * C::STG_BYTES;
+                    // the reduce that last read this staging buffer has finished reading
+                    if (leader && chunk >= NSTG)
+                        bulk_wait_group_read<NSTG - 1>();
+                    named_bar_sync(3, 128);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    st_shared_v4(sbuf + r * 128 + (((k ^ (r & 7)) & 7) << 4), u[4 * k], u[4 * k + 1],
-                                 u[4 * k + 2], u[4 * k + 3]);
-                fence_proxy_async_smem();
-                named_bar_sync(3, 128);
-                if (leader) {
-                    tma_reduce_add_3d(&tm_dqacc, sbuf, 32 * c4, m * kBlk, bh);
-                    bulk_commit_group();
+                    for (int k8 = 0; k8 < 8; ++k8)
+                        st_shared_v4(sbuf + r * 128 + (((k8 ^ (r & 7)) & 7) << 4), u[4 * k8], u[4 * k8 + 1],
+                                     u[4 * k8 + 2], u[4 * k8 + 3]);
+                    fence_proxy_async_smem();
+                    named_bar_sync(3, 128);
+                    if (leader) {
+                        tma_reduce_add_3d(&tm_dqacc, sbuf, 32 * c4, m * kBlk, bh);
+                        bulk_commit_group();
+                    }
                 }
             }
+            g += cnt;
         }
         if (leader)
             bulk_wait_group<0>();
@@ -443,140 +504,160 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = warp >> 2;
         const int r = threadIdx.x & 127;  // key row of the block == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t s_tm = tmem + lane_base + kTmS;
-        const uint32_t dp_tm = tmem + lane_base + kTmDP;
-        const bool row_valid = n * kBlk + r < N;
-        const uint32_t ds_row = sbase + C::DS_OFF + c * kSwAtomBytes + r * 128;
+        const uint32_t tm_row = tmem + lane_base;  // TMEM lane of this key row, column 0
+        // this warpgroup's 64 query columns of the dS^T tile (one swizzle block)
+        const uint32_t ds_half_smem = sbase + C::DS_OFF + c * kSwAtomBytes;
         const float2 c2 = make_float2(scale_log2, scale_log2);
-        const uint32_t ds_tm = tmem + lane_base + col_ds<D>();
         bool ok = true;
-        for (int i = 0; i < cnt; ++i) {
-            const int m = m0 + i;
-            const int s = i % QST, ds = i % DOST;
-            const uint32_t ph = static_cast<uint32_t>(i & 1);
-            ok = wait_bounded(bar(C::B_SFULL), ph, abort_flag) &&
-                 wait_bounded(bar(C::B_QFULL + s), (i / QST) & 1, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok)
-                break;
-            tc_fence_after();
-            // ---- P^T for queries [64c, 64c + 64) of this key row ----
-            const bool diag = CAUSAL && m == n;  // keys above the query are masked
-            const float *lrow = reinterpret_cast<const float *>(smem + C::L_OFF + s * kBlk * 4);
-            uint32_t pk[32];
+        int g = 0;
+        for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, bh, n); ++k) {
+            const int m0 = CAUSAL ? n : 0;
+            const int cnt = nb - m0;
+            const bool row_valid = n * kBlk + r < N;
+            for (int i = 0; i < cnt; ++i) {
+                const int gi = g + i;
+                const int s = gi % QST, ds = gi % DOST;
+                const uint32_t ph = static_cast<uint32_t>(gi & 1);
+                ok = wait_bounded(bar(C::B_SFULL), ph, abort_flag) &&
+                     wait_bounded(bar(C::B_QFULL + s), (gi / QST) & 1, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                // ---- P^T for queries [64c, 64c + 64) of this key row ----
+                // causal: the walk starts at the diagonal block m = n, where
+                // keys above the query are masked
+                const bool diag = CAUSAL && i == 0;
+                const float *lrow = reinterpret_cast<const float *>(smem + C::L_OFF + s * kBlk * 4);
+                uint32_t pk[32];
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                uint32_t u[32];
-                tmem_ld32(s_tm + 64 * c + 32 * ch, u);
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t u[32];
+                    tmem_ld32(tm_row + kTmS + 64 * c + 32 * ch, u);
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const int q = 64 * c + 32 * ch + j;
-                    const float4 l4 = *reinterpret_cast<const float4 *>(lrow + (q & ~3));
-                    const float2 l2 = (q & 2) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
-                    const float2 x = ffma2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])), c2,
-                                           make_float2(-l2.x, -l2.y));
-                    float e0 = ex2_approx(x.x);
-                    float e1 = ex2_approx(x.y);
-                    if (diag) {
-                        e0 = (q >= r) ? e0 : 0.f;
-                        e1 = (q + 1 >= r) ? e1 : 0.f;
+                    for (int j = 0; j < 32; j += 2) {
+                        const int q = 64 * c + 32 * ch + j;
+                        const float4 l4 = *reinterpret_cast<const float4 *>(lrow + (q & ~3));
+                        const float2 l2 = (q & 2) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+                        const float2 x = ffma2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])), c2,
+                                               make_float2(-l2.x, -l2.y));
+                        float e0 = ex2_approx(x.x);
+                        float e1 = ex2_approx(x.y);
+                        if (diag) {
+                            e0 = (q >= r) ? e0 : 0.f;
+                            e1 = (q + 1 >= r) ? e1 : 0.f;
+                        }
+                        pk[16 * ch + j / 2] = DTypeTraits<T>::pack(e0, e1);
                     }
-                    pk[16 * ch + j / 2] = DTypeTraits<T>::pack(e0, e1);
-                }
-                if (!row_valid) {
-                    // key past the sequence end (K row read as zeros): no weight
+                    if (!row_valid) {
+                        // key past the sequence end (K row read as zeros): no weight
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        pk[16 * ch + j] = 0u;
+                        for (int j = 0; j < 16; ++j)
+                            pk[16 * ch + j] = 0u;
+                    }
+                    tmem_st16(tm_row + kTmS + 64 * c + 16 * ch, reinterpret_cast<const uint32_t(&)[16]>(pk[16 * ch]));
                 }
-                tmem_st16(s_tm + 64 * c + 16 * ch, reinterpret_cast<const uint32_t(&)[16]>(pk[16 * ch]));
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(C::B_PFULL));
 
-            // ---- dS^T = P^T o (dP^T - D) scale, into shared memory ----
-            // D = 64: dK and dQ of the previous block (issued after this dP^T)
-            // must have finished reading dS^T before it is overwritten
-            ok = wait_bounded(bar(C::B_DPFULL), ph, abort_flag) &&
-                 wait_bounded(bar(C::B_DOFULL + ds), (i / DOST) & 1, abort_flag) &&
-                 (C::DQ_ALIAS || i == 0 || wait_bounded(bar(C::B_DQFULL), ph ^ 1u, abort_flag));
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok)
+                // ---- dS^T = P^T o (dP^T - D), into TMEM and shared memory ----
+                // D <= 64: dK and dQ of the previous block (issued after this
+                // dP^T) must have finished reading dS^T before it is overwritten
+                ok = wait_bounded(bar(C::B_DPFULL), ph, abort_flag) &&
+                     wait_bounded(bar(C::B_DOFULL + ds), (gi / DOST) & 1, abort_flag) &&
+                     (C::DQ_ALIAS || gi == 0 || wait_bounded(bar(C::B_DQFULL), ph ^ 1u, abort_flag));
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const float *drow = reinterpret_cast<const float *>(smem + C::DD_OFF + ds * kBlk * 4);
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t u[32];
+                    tmem_ld32(tm_row + kTmDP + 64 * c + 32 * ch, u);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const int q = 64 * c + 32 * ch + j;
+                        const float4 d4 = *reinterpret_cast<const float4 *>(drow + (q & ~3));
+                        const float2 dd = (q & 2) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+                        const float2 p = DTypeTraits<T>::unpack(pk[16 * ch + j / 2]);
+                        const float2 t = fadd2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])),
+                                               make_float2(-dd.x, -dd.y));
+                        // dS without the scale factor: dK and dQ apply it once at the end
+                        const float2 gr = fmul2(p, t);
+                        w[j / 2] = DTypeTraits<T>::pack(gr.x, gr.y);
+                    }
+                    // dS^T into TMEM (A operand of dK) and into shared memory
+                    // (MN-major A operand of dQ): 16-byte chunk 4 ch + k of this row
+                    // (8 queries each)
+                    tmem_st16(tm_row + col_ds<D>() + ds_half<D>() * c + 16 * ch, w);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        st_shared_v4(ds_half_smem + r * 128 + ((((4 * ch + k4) ^ (r & 7)) & 7) << 4), w[4 * k4], w[4 * k4 + 1],
+                                     w[4 * k4 + 2], w[4 * k4 + 3]);
+                }
+                fence_proxy_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(C::B_DSFULL));
+            }
+
+            // ---------------- epilogue of the item: dV_n and dK_n ----------------
+            if (ok) {
+                ok = wait_bounded(bar(C::B_DKVFULL), static_cast<uint32_t>(k & 1), abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            if (named_bar_or(1 + c, 128, !ok || *abort_flag != 0)) {
+                ok = false;
                 break;
+            }
             tc_fence_after();
-            const float *drow = reinterpret_cast<const float *>(smem + C::DD_OFF + ds * kBlk * 4);
+            // Round 32-column chunks [c0, c0 + nch) of a TMEM accumulator, stage
+            // them in this warpgroup's half of the dS^T tile (free: every product
+            // has completed, the last dQ included) and store them from column
+            // 64 * (c0 / 2).  The tile is reused by the next item's dS^T only
+            // after the store has finished reading it.
+            auto store_acc = [&](const CUtensorMap *map, uint32_t acc_col, int c0, int nch, float mul) {
+                for (int c4 = 0; c4 < nch; ++c4) {
+                    uint32_t u[32];
+                    tmem_ld32(tm_row + acc_col + 32 * (c0 + c4), u);
+                    float f[32];
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                uint32_t u[32];
-                tmem_ld32(dp_tm + 64 * c + 32 * ch, u);
-                uint32_t w[16];
+                    for (int j = 0; j < 32; ++j)
+                        f[j] = __uint_as_float(u[j]) * mul;
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const int q = 64 * c + 32 * ch + j;
-                    const float4 d4 = *reinterpret_cast<const float4 *>(drow + (q & ~3));
-                    const float2 dd = (q & 2) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
-                    const float2 p = DTypeTraits<T>::unpack(pk[16 * ch + j / 2]);
-                    const float2 t = fadd2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])),
-                                           make_float2(-dd.x, -dd.y));
-                    // dS without the scale factor: dK and dQ apply it once at the end
-                    const float2 g = fmul2(p, t);
-                    w[j / 2] = DTypeTraits<T>::pack(g.x, g.y);
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        st_shared_v4(ds_half_smem + sw128_offset(r, c4 * 4 + q4),
+                                     DTypeTraits<T>::pack(f[8 * q4 + 0], f[8 * q4 + 1]),
+                                     DTypeTraits<T>::pack(f[8 * q4 + 2], f[8 * q4 + 3]),
+                                     DTypeTraits<T>::pack(f[8 * q4 + 4], f[8 * q4 + 5]),
+                                     DTypeTraits<T>::pack(f[8 * q4 + 6], f[8 * q4 + 7]));
                 }
-                // dS^T into TMEM (A operand of dK) and into shared memory
-                // (MN-major A operand of dQ): 16-byte chunk 4 ch + k of this row
-                // (8 queries each)
-                tmem_st16(ds_tm + ds_half<D>() * c + 16 * ch, w);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    st_shared_v4(ds_row + ((((4 * ch + k) ^ (r & 7)) & 7) << 4), w[4 * k], w[4 * k + 1],
-                                 w[4 * k + 2], w[4 * k + 3]);
-            }
-            fence_proxy_async_smem();
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_DSFULL));
-        }
-
-        // ---------------- epilogue: warpgroup 0 writes dV_n, warpgroup 1 dK_n ----------------
-        if (ok) {
-            ok = wait_bounded(bar(C::B_DKVFULL), 0, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        // both staging areas are free once every product has completed: the
-        // dS^T tile (last read by dQ) and Q slot 0 (last read by dK)
-        const uint32_t stage = sbase + (c == 0 ? C::DS_OFF : C::Q_OFF);
-        const uint32_t acc_tm = tmem + lane_base + (c == 0 ? kTmDV : col_dk<D>());
-        const bool bad = named_bar_or(1 + c, 128, !ok || *abort_flag != 0);
-        if (!bad) {
-            tc_fence_after();
-#pragma unroll
+                fence_proxy_async_smem();
+                named_bar_sync(1 + c, 128);
+                if (r == 0) {
+                    tma_store_3d(map, ds_half_smem, 32 * c0, n * kBlk, bh);
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();
+                }
+                named_bar_sync(1 + c, 128);
+            };
             // dK = scale dS^T Q (dS was kept without the scale); dV as is
-            const float mul = c == 0 ? 1.f : scale;
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-                uint32_t u[32];
-                tmem_ld32(acc_tm + 32 * c4, u);
-                float f[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    f[j] = __uint_as_float(u[j]) * mul;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    st_shared_v4(stage + sw128_offset(r, c4 * 4 + q4),
-                                 DTypeTraits<T>::pack(f[8 * q4 + 0], f[8 * q4 + 1]),
-                                 DTypeTraits<T>::pack(f[8 * q4 + 2], f[8 * q4 + 3]),
-                                 DTypeTraits<T>::pack(f[8 * q4 + 4], f[8 * q4 + 5]),
-                                 DTypeTraits<T>::pack(f[8 * q4 + 6], f[8 * q4 + 7]));
+            if (D <= 64) {
+                // warpgroup 0 writes dV_n, warpgroup 1 dK_n
+                store_acc(c == 0 ? &tm_dv : &tm_dk, c == 0 ? kTmDV : col_dk<D>(), 0, D / 32, c == 0 ? 1.f : scale);
+            } else {
+                // warpgroup c writes columns [64c, 64c + 64) of both
+                const int nch = (D / 32 - 2 * c) < 2 ? (D / 32 - 2 * c) : 2;
+                store_acc(&tm_dv, kTmDV, 2 * c, nch, 1.f);
+                store_acc(&tm_dk, col_dk<D>(), 2 * c, nch, scale);
             }
-            fence_proxy_async_smem();
-            named_bar_sync(1 + c, 128);
-            if (r == 0) {
-                for (int b = 0; b < col_blocks<D>(); ++b)
-                    tma_store_3d(c == 0 ? &tm_dv : &tm_dk, stage + b * kSwAtomBytes, b * 64, n * kBlk, bh);
-                bulk_commit_group();
-                bulk_wait_group<0>();
-            }
+            g += cnt;
         }
+        if (r == 0)
+            bulk_wait_group<0>();
         tc_fence_before();
     }
 

@@ -58,6 +58,15 @@ def test_many_heads(orc, causal):
     _case(orc, 3, 3, 700, 64, "fp16", causal, 7100)
 
 
+@pytest.mark.parametrize("d,dtype", [(32, "bf16"), (64, "fp16"), (96, "fp16"), (128, "bf16")])
+@pytest.mark.parametrize("causal", [False, True])
+def test_several_items_per_cta(orc, d, dtype, causal):
+    # 2 x 40 heads x 5 key blocks = 400 (head, key block) items, more than the
+    # 152 SMs: each persistent CTA walks two or three items, so ring slots and
+    # barrier phases carry over item boundaries (causal: items of 1..5 blocks)
+    _case(orc, 2, 40, 520, d, dtype, causal, 7400 + d)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_stress_scores(orc, causal):
     # Q x 8: scaled scores with standard deviation about 8 (peaked softmax rows)
