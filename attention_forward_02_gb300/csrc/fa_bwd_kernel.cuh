@@ -109,14 +109,20 @@ template <int D>
 struct Cfg {
     static_assert(D == 32 || D == 64 || D == 96 || D == 128, "head dims 32, 64, 96, 128");
     static constexpr int TILE = kBlk * col_blocks<D>() * 128;  // one [128, D] 16-bit tile
+    // D <= 64 (CONT): two K/V buffers, so the next item's first S^T and dP^T
+    // products follow this item's last dV product like any other block's, and
+    // the dQ warpgroup writes dK_n, dV_n while the compute warps go on.
+    // D > 64: one K/V buffer (no room for two), reloaded once the item's
+    // products are done; the compute warps write dK_n, dV_n.
+    static constexpr bool CONT = D <= 64;
+    static constexpr int KVBUF = CONT ? 2 : 1;
     static constexpr int QST = D <= 64 ? 3 : 2;   // Q (+ L) ring
-    static constexpr int DOST = D <= 64 ? 3 : 1;  // dO (+ D) ring
-    static constexpr int NSTG = D <= 64 ? 2 : 1;  // dQ staging buffers
+    static constexpr int DOST = D <= 64 ? 2 : 1;  // dO (+ D) ring
+    static constexpr int NSTG = D <= 64 ? 2 : 1;  // dQ staging buffers (D <= 64: also dV_n, dK_n)
     static constexpr int STG_BYTES = kBlk * 32 * 4;  // [128 rows x 32 fp32], 128B-swizzled
     static constexpr bool DQ_ALIAS = D > 64;  // dQ (and dS^T) over the dP^T columns
-    static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + TILE;
-    static constexpr int Q_OFF = V_OFF + TILE;
+    static constexpr int KV_OFF = 0;  // buffer b: K at 2 b TILE, V at (2 b + 1) TILE
+    static constexpr int Q_OFF = KV_OFF + 2 * KVBUF * TILE;
     static constexpr int DO_OFF = Q_OFF + QST * TILE;
     static constexpr int DS_OFF = DO_OFF + DOST * TILE;  // dS^T [128 keys x 128 queries]
     static constexpr int STG_OFF = DS_OFF + kBlk * kBlk * 2;
@@ -124,8 +130,8 @@ struct Cfg {
     static constexpr int DD_OFF = L_OFF + QST * kBlk * 4;      // DOST x 128 fp32
     static constexpr int BAR_OFF = DD_OFF + DOST * kBlk * 4;
     static constexpr int B_KVFULL = 0;
-    static constexpr int B_KVEMPTY = 1;
-    static constexpr int B_QFULL = 2;
+    static constexpr int B_KVEMPTY = B_KVFULL + KVBUF;
+    static constexpr int B_QFULL = B_KVEMPTY + KVBUF;
     static constexpr int B_QEMPTY = B_QFULL + QST;
     static constexpr int B_DOFULL = B_QEMPTY + QST;
     static constexpr int B_DOEMPTY = B_DOFULL + DOST;
@@ -136,13 +142,15 @@ struct Cfg {
     static constexpr int B_DQFULL = B_DSFULL + 1;
     static constexpr int B_DQFREE = B_DQFULL + 1;
     static constexpr int B_DKVFULL = B_DQFREE + 1;
-    static constexpr int B_DRAIN = B_DKVFULL + 1;
+    static constexpr int B_DKVFREE = B_DKVFULL + 1;  // CONT: dK_n, dV_n read out of TMEM
+    static constexpr int B_DRAIN = B_DKVFREE + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SLOT_OFF = BAR_OFF + 8 * NUM_BARS;  // TMEM base address, abort flag
     static constexpr int SMEM_USED = SLOT_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(DS_OFF % 1024 == 0 && STG_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    static_assert(!CONT || (NSTG == 2 && STG_BYTES == kBlk * 128), "dV_n, dK_n staged in the two dQ buffers");
 };
 
 // Work item number w: (head bh, key block n).  Causal: the heaviest key
@@ -188,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float scale_log2)
 {
     using C = Cfg<D>;
+    constexpr bool CONT = C::CONT;
+    constexpr int KVBUF = C::KVBUF;
     constexpr int QST = C::QST;
     constexpr int DOST = C::DOST;
     constexpr int NSTG = C::NSTG;
@@ -208,8 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SLOT_OFF + 4);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_KVFULL), 1);
-        mbar_init(bar(C::B_KVEMPTY), 1);
+        for (int b = 0; b < KVBUF; ++b) {
+            mbar_init(bar(C::B_KVFULL + b), 1);
+            mbar_init(bar(C::B_KVEMPTY + b), 1);
+        }
         for (int s = 0; s < QST; ++s) {
             mbar_init(bar(C::B_QFULL + s), 1);
             mbar_init(bar(C::B_QEMPTY + s), 1);
@@ -225,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::B_DQFULL), 1);
         mbar_init(bar(C::B_DQFREE), 128);
         mbar_init(bar(C::B_DKVFULL), 1);
+        mbar_init(bar(C::B_DKVFREE), 128);
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -278,25 +291,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int m0 = CAUSAL ? n : 0;  // first query block that sees key block n
                 const int cnt = nb - m0;        // query blocks walked (>= 1)
                 // the first query block ahead of K_n, V_n: its ring slots free up
-                // before the previous item's last products have read K and V
+                // before the products of the item that last used this K/V buffer
+                // have all read K and V
                 if (!(ok = load_block(m0)))
                     break;
-                if (k > 0 && !(ok = wait_bounded(bar(C::B_KVEMPTY), (k - 1) & 1, abort_flag)))
+                const int kb = k % KVBUF;
+                if (k >= KVBUF && !(ok = wait_bounded(bar(C::B_KVEMPTY + kb), ((k / KVBUF) - 1) & 1, abort_flag)))
                     break;
-                mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE);
+                mbar_arrive_expect_tx(bar(C::B_KVFULL + kb), 2 * C::TILE);
                 for (int b = 0; b < col_blocks<D>(); ++b) {
-                    tma_load_3d(sbase + C::K_OFF + b * kSwAtomBytes, &tm_k, bar(C::B_KVFULL), b * 64, n * kBlk,
-                                bh, pol_kv);
-                    tma_load_3d(sbase + C::V_OFF + b * kSwAtomBytes, &tm_v, bar(C::B_KVFULL), b * 64, n * kBlk,
-                                bh, pol_kv);
+                    tma_load_3d(sbase + C::KV_OFF + (2 * kb) * C::TILE + b * kSwAtomBytes, &tm_k,
+                                bar(C::B_KVFULL + kb), b * 64, n * kBlk, bh, pol_kv);
+                    tma_load_3d(sbase + C::KV_OFF + (2 * kb + 1) * C::TILE + b * kSwAtomBytes, &tm_v,
+                                bar(C::B_KVFULL + kb), b * 64, n * kBlk, bh, pol_kv);
                 }
                 ++nkv;
                 for (int i = 1; ok && i < cnt; ++i)
                     ok = load_block(m0 + i);
             }
             // wait for every copy this thread issued
-            if (nkv > 0)
-                drain_bounded(bar(C::B_KVFULL), (nkv - 1) & 1);
+            for (int b = 0; b < KVBUF; ++b)
+                if (nkv > b)
+                    drain_bounded(bar(C::B_KVFULL + b), ((nkv - 1 - b) / KVBUF) & 1);
             for (int s = 0; s < QST; ++s)
                 if (nq > s)
                     drain_bounded(bar(C::B_QFULL + s), ((nq - 1 - s) / QST) & 1);
@@ -312,10 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_acc = make_idesc_f16(BF, kBlk, D, false, true);
             constexpr uint32_t idesc_dq = make_idesc_f16(BF, kBlk, D, true, true);
             // K-major views (operands whose contraction runs along the row) and
-            // MN-major views (contraction down the rows) of the same tiles.
-            const uint64_t k_kmaj = make_sdesc_sw128(sbase + C::K_OFF, 16, 1024);
-            const uint64_t k_mn = make_sdesc_sw128(sbase + C::K_OFF, kSwAtomBytes, 1024);
-            const uint64_t v_kmaj = make_sdesc_sw128(sbase + C::V_OFF, 16, 1024);
+            // MN-major views (contraction down the rows) of the same tiles; K/V
+            // buffer b is 2 b TILE bytes further on.
+            const uint64_t k_kmaj = make_sdesc_sw128(sbase + C::KV_OFF, 16, 1024);
+            const uint64_t k_mn = make_sdesc_sw128(sbase + C::KV_OFF, kSwAtomBytes, 1024);
+            const uint64_t v_kmaj = make_sdesc_sw128(sbase + C::KV_OFF + C::TILE, 16, 1024);
             const uint64_t q_kmaj = make_sdesc_sw128(sbase + C::Q_OFF, 16, 1024);
             const uint64_t q_mn = make_sdesc_sw128(sbase + C::Q_OFF, kSwAtomBytes, 1024);
             const uint64_t do_kmaj = make_sdesc_sw128(sbase + C::DO_OFF, 16, 1024);
@@ -329,17 +346,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto mn = [](int kk) -> uint32_t { return static_cast<uint32_t>((kk * 2048) >> 4); };
             auto tile = [](int slot) -> uint32_t { return static_cast<uint32_t>((slot * C::TILE) >> 4); };
+            auto kvbuf = [](int b) -> uint32_t { return static_cast<uint32_t>((2 * b * C::TILE) >> 4); };
 
-            auto issue_s = [&](int s) {  // S^T = K Q^T
+            auto issue_s = [&](int s, int b) {  // S^T = K Q^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    umma_f16_ss(tmem + kTmS, k_kmaj + kmaj(kk), q_kmaj + tile(s) + kmaj(kk), idesc_s,
+                    umma_f16_ss(tmem + kTmS, k_kmaj + kvbuf(b) + kmaj(kk), q_kmaj + tile(s) + kmaj(kk), idesc_s,
                                 kk > 0 ? 1u : 0u);
             };
-            auto issue_dp = [&](int s) {  // dP^T = V dO^T
+            auto issue_dp = [&](int s, int b) {  // dP^T = V dO^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    umma_f16_ss(tmem + kTmDP, v_kmaj + kmaj(kk), do_kmaj + tile(s) + kmaj(kk), idesc_s,
+                    umma_f16_ss(tmem + kTmDP, v_kmaj + kvbuf(b) + kmaj(kk), do_kmaj + tile(s) + kmaj(kk), idesc_s,
                                 kk > 0 ? 1u : 0u);
             };
             auto issue_dv = [&](int s, bool acc) {  // dV += P^T dO
@@ -354,67 +372,84 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_f16_ts(tmem + col_dk<D>(), tmem + col_ds<D>() + tm_p_step(kk, ds_half<D>()), q_mn + tile(s) + mn(kk),
                                 idesc_acc, (acc || kk > 0) ? 1u : 0u);
             };
-            auto issue_dq = [&]() {  // dQ = dS K
+            auto issue_dq = [&](int b) {  // dQ = dS K
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 16; ++kk)
-                    umma_f16_ss(tmem + col_dq<D>(), ds_mn + mn(kk), k_mn + mn(kk), idesc_dq, kk > 0 ? 1u : 0u);
+                    umma_f16_ss(tmem + col_dq<D>(), ds_mn + mn(kk), k_mn + kvbuf(b) + mn(kk), idesc_dq,
+                                kk > 0 ? 1u : 0u);
+            };
+            // S^T and dP^T of global block gq, whose K/V sit in buffer b.  The
+            // previous block's dV product, issued earlier, has read P^T from
+            // the S^T columns; D > 64: the previous block's dQ, in the dP^T
+            // columns, must have been read out first.
+            auto start_block = [&](int gq, int b) -> bool {
+                if (!wait_bounded(bar(C::B_QFULL + gq % QST), (gq / QST) & 1, abort_flag))
+                    return false;
+                tc_fence_after();
+                issue_s(gq % QST, b);
+                umma_commit(bar(C::B_SFULL));
+                return true;
+            };
+            auto start_dp = [&](int gq, int b) -> bool {
+                if (!((!C::DQ_ALIAS || gq == 0 || wait_bounded(bar(C::B_DQFREE), (gq - 1) & 1, abort_flag)) &&
+                      wait_bounded(bar(C::B_DOFULL + gq % DOST), (gq / DOST) & 1, abort_flag)))
+                    return false;
+                tc_fence_after();
+                issue_dp(gq % DOST, b);
+                umma_commit(bar(C::B_DPFULL));
+                return true;
             };
 
             bool ok = true;
             int g = 0;
-            for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, bh, n); ++k) {
+            bool have = item_of<CAUSAL>(0, BH, nb, bh, n);
+            // the first item's first block (CONT: every later item's first
+            // block starts inside the previous item's last block)
+            if (have)
+                ok = wait_bounded(bar(C::B_KVFULL), 0, abort_flag) && start_block(0, 0) && start_dp(0, 0);
+            for (int k = 0; ok && have; ++k) {
                 const int cnt = nb - (CAUSAL ? n : 0);
-                // S^T of the item's first block: the previous item's last dV
-                // product, issued earlier, has read P^T from these columns
-                if (!(ok = wait_bounded(bar(C::B_KVFULL), k & 1, abort_flag) &&
-                           wait_bounded(bar(C::B_QFULL + g % QST), (g / QST) & 1, abort_flag)))
-                    break;
-                tc_fence_after();
-                issue_s(g % QST);
-                umma_commit(bar(C::B_SFULL));
-                // D > 64: the previous block's dQ sits in the dP^T columns until
-                // warps 8-11 have read it out
-                if (!(ok = (!C::DQ_ALIAS || g == 0 || wait_bounded(bar(C::B_DQFREE), (g - 1) & 1, abort_flag)) &&
-                           wait_bounded(bar(C::B_DOFULL + g % DOST), (g / DOST) & 1, abort_flag)))
-                    break;
-                tc_fence_after();
-                issue_dp(g % DOST);
-                umma_commit(bar(C::B_DPFULL));
+                const int kb = k % KVBUF;
+                int bh1 = 0, n1 = 0;
+                const bool have_next = item_of<CAUSAL>(k + 1, BH, nb, bh1, n1);
                 for (int i = 0; ok && i < cnt; ++i) {
                     const int gi = g + i;
                     const int s = gi % QST, ds = gi % DOST;
                     const uint32_t ph = static_cast<uint32_t>(gi & 1);
-                    // (block 0: the compute warps arrive here after reading the
-                    // previous item's dV and dK out of TMEM, so they may be reset)
+                    // next block: in this item, or (CONT) the next item's first
+                    const bool next_here = i + 1 < cnt;
+                    const bool next_cross = CONT && !next_here && have_next;
+                    const int kb1 = next_here ? kb : (k + 1) % KVBUF;
                     if (!(ok = wait_bounded(bar(C::B_PFULL), ph, abort_flag)))
+                        break;
+                    // CONT, block 0: dV_n, dK_n of the previous item are read
+                    // out of TMEM before this item's first products reset them
+                    // (otherwise the compute warps' epilogue, ahead of this P^T,
+                    // has read them)
+                    if (CONT && i == 0 && k > 0 && !(ok = wait_bounded(bar(C::B_DKVFREE), (k - 1) & 1, abort_flag)))
                         break;
                     tc_fence_after();
                     issue_dv(ds, i > 0);
-                    if (i + 1 < cnt) {
+                    if (next_here || next_cross) {
                         // S^T of the next block overwrites P^T, after the dV product
                         // above has read it (one thread's MMAs run in issue order)
-                        const int s1 = (gi + 1) % QST;
-                        if (!(ok = wait_bounded(bar(C::B_QFULL + s1), ((gi + 1) / QST) & 1, abort_flag)))
+                        if (next_cross &&
+                            !(ok = wait_bounded(bar(C::B_KVFULL + kb1), ((k + 1) / KVBUF) & 1, abort_flag)))
                             break;
-                        tc_fence_after();
-                        issue_s(s1);
-                        umma_commit(bar(C::B_SFULL));
+                        if (!(ok = start_block(gi + 1, kb1)))
+                            break;
                     }
                     if (!(ok = wait_bounded(bar(C::B_DSFULL), ph, abort_flag)))
                         break;
                     tc_fence_after();
                     // the compute warps are done with D_m; dP^T and dV have read dO_m
                     umma_commit(bar(C::B_DOEMPTY + ds));
-                    const int ds1 = (gi + 1) % DOST;
-                    if (!C::DQ_ALIAS && i + 1 < cnt) {
+                    if (!C::DQ_ALIAS && (next_here || next_cross)) {
                         // D <= 64: dP^T of the next block first (its columns are
                         // free: dS^T has columns of its own), so the compute warps
                         // can go on
-                        if (!(ok = wait_bounded(bar(C::B_DOFULL + ds1), ((gi + 1) / DOST) & 1, abort_flag)))
+                        if (!(ok = start_dp(gi + 1, kb1)))
                             break;
-                        tc_fence_after();
-                        issue_dp(ds1);
-                        umma_commit(bar(C::B_DPFULL));
                     }
                     // D > 64: dK reads dS^T from the dP^T columns before dQ writes
                     // them (one thread's MMAs run in issue order)
@@ -424,33 +459,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         tc_fence_after();
                     }
-                    issue_dq();
+                    issue_dq(kb);
                     umma_commit(bar(C::B_DQFULL));
                     umma_commit(bar(C::B_QEMPTY + s));
-                    if (C::DQ_ALIAS && i + 1 < cnt) {
-                        // dQ_m sits in the dP^T columns: wait until it is read out
-                        if (!(ok = wait_bounded(bar(C::B_DQFREE), ph, abort_flag) &&
-                                   wait_bounded(bar(C::B_DOFULL + ds1), ((gi + 1) / DOST) & 1, abort_flag)))
+                    if (C::DQ_ALIAS && next_here) {
+                        // dQ_m sits in the dP^T columns: start_dp waits until it is read out
+                        if (!(ok = start_dp(gi + 1, kb)))
                             break;
-                        tc_fence_after();
-                        issue_dp(ds1);
-                        umma_commit(bar(C::B_DPFULL));
                     }
                 }
                 if (!ok)
                     break;
                 // dK_n, dV_n are final; K_n, V_n are no longer read
                 umma_commit(bar(C::B_DKVFULL));
-                umma_commit(bar(C::B_KVEMPTY));
+                umma_commit(bar(C::B_KVEMPTY + kb));
                 g += cnt;
+                if (!CONT && have_next) {
+                    // the next item's K, V land once the products above are done
+                    bh = bh1;
+                    n = n1;
+                    ok = wait_bounded(bar(C::B_KVFULL), (k + 1) & 1, abort_flag) && start_block(g, 0) &&
+                         start_dp(g, 0);
+                }
+                bh = bh1;
+                n = n1;
+                have = have_next;
             }
             // every MMA this thread issued has completed once this arrives
             umma_commit(bar(C::B_DRAIN));
             drain_bounded(bar(C::B_DRAIN), 0);
         }
     } else if (warp >= kDqWarp0 && warp < kDqWarp0 + 4) {
-        // ---------------- dQ warpgroup ----------------
-        const int r = threadIdx.x & 127;  // query row of the block == TMEM lane
+        // ---------------- dQ warpgroup (CONT: also dK_n, dV_n) ----------------
+        const int r = threadIdx.x & 127;  // query row of the block == TMEM lane (dK/dV: key row)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t dq_tm = tmem + lane_base + col_dq<D>();
         const bool leader = threadIdx.x == kDqWarp0 * 32;
@@ -496,6 +537,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             g += cnt;
+            if constexpr (CONT) {
+                if (!ok)
+                    break;
+                // ---- dV_n and dK_n of the item (D <= 64: one 64-column block each) ----
+                bool w = wait_bounded(bar(C::B_DKVFULL), static_cast<uint32_t>(k & 1), abort_flag);
+                w = __all_sync(0xffffffffu, w);
+                if (named_bar_or(3, 128, !w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // staged in the two dQ buffers once every earlier reduce has read
+                // them: 32 columns at a time out of TMEM, rounded (dK = scale
+                // dS^T Q: dS was kept without the scale); then TMEM is free for
+                // the next item's first products
+                const uint32_t sv = sbase + C::STG_OFF;
+                const uint32_t sk = sv + C::STG_BYTES;
+                if (leader)
+                    bulk_wait_group_read<0>();
+                named_bar_sync(3, 128);
+#pragma unroll 1
+                for (int t = 0; t < 2 * (D / 32); ++t) {
+                    const int c4 = t >> 1;
+                    const bool is_k = (t & 1) != 0;
+                    const float mul = is_k ? scale : 1.f;
+                    uint32_t u[32];
+                    tmem_ld32(tmem + lane_base + (is_k ? col_dk<D>() : kTmDV) + 32 * c4, u);
+                    const uint32_t dst = is_k ? sk : sv;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        st_shared_v4(dst + sw128_offset(r, 4 * c4 + q4),
+                                     DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 0]) * mul, __uint_as_float(u[8 * q4 + 1]) * mul),
+                                     DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 2]) * mul, __uint_as_float(u[8 * q4 + 3]) * mul),
+                                     DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 4]) * mul, __uint_as_float(u[8 * q4 + 5]) * mul),
+                                     DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 6]) * mul, __uint_as_float(u[8 * q4 + 7]) * mul));
+                }
+                tc_fence_before();
+                mbar_arrive(bar(C::B_DKVFREE));
+                fence_proxy_async_smem();
+                named_bar_sync(3, 128);
+                if (leader) {
+                    tma_store_3d(&tm_dv, sv, 0, n * kBlk, bh);
+                    tma_store_3d(&tm_dk, sk, 0, n * kBlk, bh);
+                    bulk_commit_group();
+                    // the next dQ chunks reuse both buffers
+                    bulk_wait_group_read<0>();
+                }
+                named_bar_sync(3, 128);
+            }
         }
         if (leader)
             bulk_wait_group<0>();
@@ -603,60 +693,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(bar(C::B_DSFULL));
             }
-
-            // ---------------- epilogue of the item: dV_n and dK_n ----------------
-            if (ok) {
-                ok = wait_bounded(bar(C::B_DKVFULL), static_cast<uint32_t>(k & 1), abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-            }
-            if (named_bar_or(1 + c, 128, !ok || *abort_flag != 0)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // Round 32-column chunks [c0, c0 + nch) of a TMEM accumulator, stage
-            // them in this warpgroup's half of the dS^T tile (free: every product
-            // has completed, the last dQ included) and store them from column
-            // 64 * (c0 / 2).  The tile is reused by the next item's dS^T only
-            // after the store has finished reading it.
-            auto store_acc = [&](const CUtensorMap *map, uint32_t acc_col, int c0, int nch, float mul) {
-                for (int c4 = 0; c4 < nch; ++c4) {
-                    uint32_t u[32];
-                    tmem_ld32(tm_row + acc_col + 32 * (c0 + c4), u);
-                    float f[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        f[j] = __uint_as_float(u[j]) * mul;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        st_shared_v4(ds_half_smem + sw128_offset(r, c4 * 4 + q4),
-                                     DTypeTraits<T>::pack(f[8 * q4 + 0], f[8 * q4 + 1]),
-                                     DTypeTraits<T>::pack(f[8 * q4 + 2], f[8 * q4 + 3]),
-                                     DTypeTraits<T>::pack(f[8 * q4 + 4], f[8 * q4 + 5]),
-                                     DTypeTraits<T>::pack(f[8 * q4 + 6], f[8 * q4 + 7]));
+            g += cnt;
+            if constexpr (!CONT) {
+                // ---------------- epilogue of the item: dV_n and dK_n ----------------
+                if (ok) {
+                    ok = wait_bounded(bar(C::B_DKVFULL), static_cast<uint32_t>(k & 1), abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
                 }
-                fence_proxy_async_smem();
-                named_bar_sync(1 + c, 128);
-                if (r == 0) {
-                    tma_store_3d(map, ds_half_smem, 32 * c0, n * kBlk, bh);
-                    bulk_commit_group();
-                    bulk_wait_group_read<0>();
+                if (named_bar_or(1 + c, 128, !ok || *abort_flag != 0)) {
+                    ok = false;
+                    break;
                 }
-                named_bar_sync(1 + c, 128);
-            };
-            // dK = scale dS^T Q (dS was kept without the scale); dV as is
-            if (D <= 64) {
-                // warpgroup 0 writes dV_n, warpgroup 1 dK_n
-                store_acc(c == 0 ? &tm_dv : &tm_dk, c == 0 ? kTmDV : col_dk<D>(), 0, D / 32, c == 0 ? 1.f : scale);
-            } else {
-                // warpgroup c writes columns [64c, 64c + 64) of both
+                tc_fence_after();
+                // Round 32-column chunks [c0, c0 + nch) of a TMEM accumulator, stage
+                // them in this warpgroup's half of the dS^T tile (free: every product
+                // has completed, the last dQ included) and store them from column
+                // 32 c0.  The tile is reused by the next item's dS^T only after the
+                // store has finished reading it.
+                auto store_acc = [&](const CUtensorMap *map, uint32_t acc_col, int c0, int nch, float mul) {
+                    for (int c4 = 0; c4 < nch; ++c4) {
+                        uint32_t u[32];
+                        tmem_ld32(tm_row + acc_col + 32 * (c0 + c4), u);
+                        float f[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            f[j] = __uint_as_float(u[j]) * mul;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            st_shared_v4(ds_half_smem + sw128_offset(r, c4 * 4 + q4),
+                                         DTypeTraits<T>::pack(f[8 * q4 + 0], f[8 * q4 + 1]),
+                                         DTypeTraits<T>::pack(f[8 * q4 + 2], f[8 * q4 + 3]),
+                                         DTypeTraits<T>::pack(f[8 * q4 + 4], f[8 * q4 + 5]),
+                                         DTypeTraits<T>::pack(f[8 * q4 + 6], f[8 * q4 + 7]));
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(1 + c, 128);
+                    if (r == 0) {
+                        tma_store_3d(map, ds_half_smem, 32 * c0, n * kBlk, bh);
+                        bulk_commit_group();
+                        bulk_wait_group_read<0>();
+                    }
+                    named_bar_sync(1 + c, 128);
+                };
+                // dK = scale dS^T Q (dS was kept without the scale); dV as is.
+                // Warpgroup c writes columns [64c, 64c + 64) of both.
                 const int nch = (D / 32 - 2 * c) < 2 ? (D / 32 - 2 * c) : 2;
                 store_acc(&tm_dv, kTmDV, 2 * c, nch, 1.f);
                 store_acc(&tm_dk, col_dk<D>(), 2 * c, nch, scale);
             }
-            g += cnt;
         }
-        if (r == 0)
+        if (!CONT && r == 0)
             bulk_wait_group<0>();
         tc_fence_before();
     }
