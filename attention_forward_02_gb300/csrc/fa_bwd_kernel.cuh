@@ -454,6 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // D > 64: dK reads dS^T from the dP^T columns before dQ writes
                     // them (one thread's MMAs run in issue order)
                     issue_dk(s, i > 0);
+                    // CONT: dK_n, dV_n are final once this dK product is done; the
+                    // dQ warpgroup writes them while dQ_m runs
+                    if (CONT && !next_here)
+                        umma_commit(bar(C::B_DKVFULL));
                     if (!C::DQ_ALIAS && gi > 0) {
                         if (!(ok = wait_bounded(bar(C::B_DQFREE), (gi - 1) & 1, abort_flag)))
                             break;
@@ -470,8 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok)
                     break;
-                // dK_n, dV_n are final; K_n, V_n are no longer read
-                umma_commit(bar(C::B_DKVFULL));
+                // dK_n, dV_n are final (D > 64: the compute warps then stage them
+                // in the dS^T tile, which the last dQ product has read); K_n, V_n
+                // are no longer read
+                if (!CONT)
+                    umma_commit(bar(C::B_DKVFULL));
                 umma_commit(bar(C::B_KVEMPTY + kb));
                 g += cnt;
                 if (!CONT && have_next) {
@@ -501,6 +508,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int m0 = CAUSAL ? n : 0;
             const int cnt = nb - m0;
             for (int i = 0; i < cnt; ++i) {
+                bool after_epilogue = false;
+                if (CONT && i + 1 == cnt) {
+                    // ---- dV_n and dK_n of the item (one 64-column block each),
+                    // final once the last dK product is done (before the last dQ) ----
+                    bool w = wait_bounded(bar(C::B_DKVFULL), static_cast<uint32_t>(k & 1), abort_flag);
+                    w = __all_sync(0xffffffffu, w);
+                    if (named_bar_or(3, 128, !w)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // staged in the two dQ buffers once the earlier reduces have
+                    // read them, 32 columns at a time, rounded (dK = scale dS^T Q:
+                    // dS was kept without the scale); then TMEM is free for the
+                    // next item's first products
+                    const uint32_t sv = sbase + C::STG_OFF;
+                    const uint32_t sk = sv + C::STG_BYTES;
+                    if (leader)
+                        bulk_wait_group_read<0>();
+                    named_bar_sync(3, 128);
+#pragma unroll 1
+                    for (int t = 0; t < 2 * (D / 32); ++t) {
+                        const int c4 = t >> 1;
+                        const bool is_k = (t & 1) != 0;
+                        const float mul = is_k ? scale : 1.f;
+                        uint32_t u[32];
+                        tmem_ld32(tmem + lane_base + (is_k ? col_dk<D>() : kTmDV) + 32 * c4, u);
+                        const uint32_t dst = is_k ? sk : sv;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            st_shared_v4(dst + sw128_offset(r, 4 * c4 + q4),
+                                         DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 0]) * mul, __uint_as_float(u[8 * q4 + 1]) * mul),
+                                         DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 2]) * mul, __uint_as_float(u[8 * q4 + 3]) * mul),
+                                         DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 4]) * mul, __uint_as_float(u[8 * q4 + 5]) * mul),
+                                         DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 6]) * mul, __uint_as_float(u[8 * q4 + 7]) * mul));
+                    }
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_DKVFREE));
+                    fence_proxy_async_smem();
+                    named_bar_sync(3, 128);
+                    if (leader) {
+                        tma_store_3d(&tm_dv, sv, 0, n * kBlk, bh);
+                        tma_store_3d(&tm_dk, sk, 0, n * kBlk, bh);
+                        bulk_commit_group();
+                    }
+                    after_epilogue = true;  // the next staging waits for these stores
+                }
                 bool w = wait_bounded(bar(C::B_DQFULL), static_cast<uint32_t>((g + i) & 1), abort_flag);
                 w = __all_sync(0xffffffffu, w);
                 if (named_bar_or(3, 128, !w)) {
@@ -520,8 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int stg = chunk % NSTG;
                     const uint32_t sbuf = sbase + C::STG_OFF + stg * C::STG_BYTES;
-                    // the reduce that last read this staging buffer has finished reading
-                    if (leader && chunk >= NSTG)
+                    // the reduce (or, right after the epilogue, the dV_n / dK_n
+                    // stores) that last read this staging buffer has finished reading
+                    if (leader && after_epilogue && c4 == 0)
+                        bulk_wait_group_read<0>();
+                    else if (leader && chunk >= NSTG)
                         bulk_wait_group_read<NSTG - 1>();
                     named_bar_sync(3, 128);
 #pragma unroll
@@ -537,55 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             g += cnt;
-            if constexpr (CONT) {
-                if (!ok)
-                    break;
-                // ---- dV_n and dK_n of the item (D <= 64: one 64-column block each) ----
-                bool w = wait_bounded(bar(C::B_DKVFULL), static_cast<uint32_t>(k & 1), abort_flag);
-                w = __all_sync(0xffffffffu, w);
-                if (named_bar_or(3, 128, !w)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // staged in the two dQ buffers once every earlier reduce has read
-                // them: 32 columns at a time out of TMEM, rounded (dK = scale
-                // dS^T Q: dS was kept without the scale); then TMEM is free for
-                // the next item's first products
-                const uint32_t sv = sbase + C::STG_OFF;
-                const uint32_t sk = sv + C::STG_BYTES;
-                if (leader)
-                    bulk_wait_group_read<0>();
-                named_bar_sync(3, 128);
-#pragma unroll 1
-                for (int t = 0; t < 2 * (D / 32); ++t) {
-                    const int c4 = t >> 1;
-                    const bool is_k = (t & 1) != 0;
-                    const float mul = is_k ? scale : 1.f;
-                    uint32_t u[32];
-                    tmem_ld32(tmem + lane_base + (is_k ? col_dk<D>() : kTmDV) + 32 * c4, u);
-                    const uint32_t dst = is_k ? sk : sv;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        st_shared_v4(dst + sw128_offset(r, 4 * c4 + q4),
-                                     DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 0]) * mul, __uint_as_float(u[8 * q4 + 1]) * mul),
-                                     DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 2]) * mul, __uint_as_float(u[8 * q4 + 3]) * mul),
-                                     DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 4]) * mul, __uint_as_float(u[8 * q4 + 5]) * mul),
-                                     DTypeTraits<T>::pack(__uint_as_float(u[8 * q4 + 6]) * mul, __uint_as_float(u[8 * q4 + 7]) * mul));
-                }
-                tc_fence_before();
-                mbar_arrive(bar(C::B_DKVFREE));
-                fence_proxy_async_smem();
-                named_bar_sync(3, 128);
-                if (leader) {
-                    tma_store_3d(&tm_dv, sv, 0, n * kBlk, bh);
-                    tma_store_3d(&tm_dk, sk, 0, n * kBlk, bh);
-                    bulk_commit_group();
-                    // the next dQ chunks reuse both buffers
-                    bulk_wait_group_read<0>();
-                }
-                named_bar_sync(3, 128);
-            }
         }
         if (leader)
             bulk_wait_group<0>();
