@@ -48,6 +48,7 @@ METRIC = "attention fwd TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
 METRIC_BWD = "attention bwd TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor peak"
 METRIC_DEC = "decoding attention K/V GB/s at 1 GB300 and % of measured HBM bandwidth"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+EX2_PER_CLOCK_PER_SM = 31.3  # measured ex2.approx.ftz.f32 rate (see the exp diagnostic below)
 
 
 def parse_args():
@@ -291,11 +292,21 @@ class OracleTimer:
         return max(1, min(total, int(seconds / per_row)))
 
 
+def oracle_full_flops(meta, variants):
+    """The oracle's own fp64 work for every row of the workload (causal row i sees i + 1 keys)."""
+    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+    return sum((2.0 * B * H * N * (N + 1) * d) if c else (4.0 * B * H * N * N * d) for c in variants)
+
+
 def cpu_baseline_obj(timer, seconds, seed=99):
     n = timer.rows_for_seconds(seconds)
     rows = oracle_sample_rows(timer.meta, n, seed=seed)
     dt, flops = timer.run(rows)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+    rate = flops / dt
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": timer.threads, "kind": "oracle",
+            "rows_per_s": len(rows) * len(timer.variants) / dt,
+            # not measured: the whole workload's oracle work at the sample's rate
+            "extrapolated_full_s": oracle_full_flops(timer.meta, timer.variants) / rate,
             "sample": "%d random query rows of workload %s (of %d), variants %s, fp64 C oracle, "
                       "%.1f s" % (len(rows), timer.meta["name"],
                                    timer.meta["B"] * timer.meta["H"] * timer.meta["N"],
@@ -496,6 +507,19 @@ def main():
                 "variants_tflops": {("causal" if c else "noncausal"):
                                     flops_of(meta, c) / (statistics.mean(per_kernel_ms[j]) / 1e3)
                                     / 1e12 for j, c in enumerate(variants)}}
+
+    # Secondary limit at small head dims: one 2^x per score on the MUFU, against
+    # 31.3 ex2.approx.ftz.f32 per clock per SM (a microbenchmark of 152 CTAs x
+    # 512 threads on this GPU model; 38.6 when mixed 2:1 with the f32 -> f16x2
+    # conversion) at the median SM clock of the timed region.
+    exps = float(meta["B"] * meta["H"] * meta["N"] * meta["N"]) * (0.5 if dom_causal else 1.0)
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    ex2_peak = EX2_PER_CLOCK_PER_SM * sm_count * sm_mhz * 1e6
+    roofline["exp_diagnostic"] = {"exps_per_launch": exps, "achieved_per_s": exps / (dom_ms / 1e3),
+                                  "ex2_peak_per_s": ex2_peak, "frac": exps / (dom_ms / 1e3) / ex2_peak,
+                                  "peak_source": "microbenchmark, %.1f per clock per SM x %d SMs x %.0f MHz"
+                                                 % (EX2_PER_CLOCK_PER_SM, sm_count, sm_mhz)}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
