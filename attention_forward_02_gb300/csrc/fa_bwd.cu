@@ -50,18 +50,21 @@ void init_bwd(BwdState &st)
 
 long long padded_rows(int N) { return (static_cast<long long>(N) + fa::bwd::kBlk - 1) / fa::bwd::kBlk * fa::bwd::kBlk; }
 
-// fp32 accumulator [BH, Npad, d]: box 32 columns (128 bytes) x 128 rows x 1,
-// SWIZZLE_128B (the layout the dQ warps stage).
+// fp32 accumulator [BH, Npad, d], in the layout the dQ warps stage: box
+// 32 columns (128 bytes) x 128 rows x 1 with SWIZZLE_128B for d <= 64, box
+// 16 columns (64 bytes) x 128 rows x 1 with SWIZZLE_64B for d > 64.
 fa_status_t encode_acc_map(EncodeTiledFn encode, CUtensorMap *map, float *ptr, int BH, long long Npad, int d)
 {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Npad),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                                    static_cast<cuuint64_t>(Npad) * static_cast<cuuint64_t>(d) * 4};
-    const cuuint32_t box[3] = {32, 128, 1};
+    const bool narrow = d > 64;
+    const cuuint32_t box[3] = {narrow ? 16u : 32u, 128, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }

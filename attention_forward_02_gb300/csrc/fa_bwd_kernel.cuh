@@ -118,8 +118,14 @@ struct Cfg {
     static constexpr int KVBUF = CONT ? 2 : 1;
     static constexpr int QST = D <= 64 ? 3 : 2;   // Q (+ L) ring
     static constexpr int DOST = D <= 64 ? 2 : 1;  // dO (+ D) ring
-    static constexpr int NSTG = D <= 64 ? 2 : 1;  // dQ staging buffers (D <= 64: also dV_n, dK_n)
-    static constexpr int STG_BYTES = kBlk * 32 * 4;  // [128 rows x 32 fp32], 128B-swizzled
+    // dQ goes to the fp32 accumulator in chunks of DQ_COLS columns through two
+    // staging buffers, so that one reduce-add can read its buffer while the
+    // next chunk is staged: [128 rows x 32 fp32] 128B-swizzled (D <= 64, where
+    // the buffers also carry dV_n, dK_n), [128 rows x 16 fp32] 64B-swizzled
+    // (D > 64, where shared memory has room for 16 KB of staging only).
+    static constexpr int NSTG = 2;
+    static constexpr int DQ_COLS = D <= 64 ? 32 : 16;
+    static constexpr int STG_BYTES = kBlk * DQ_COLS * 4;
     static constexpr bool DQ_ALIAS = D > 64;  // dQ (and dS^T) over the dP^T columns
     static constexpr int KV_OFF = 0;  // buffer b: K at 2 b TILE, V at (2 b + 1) TILE
     static constexpr int Q_OFF = KV_OFF + 2 * KVBUF * TILE;
@@ -151,6 +157,7 @@ struct Cfg {
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(DS_OFF % 1024 == 0 && STG_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
     static_assert(!CONT || (NSTG == 2 && STG_BYTES == kBlk * 128), "dV_n, dK_n staged in the two dQ buffers");
+    static_assert(32 % DQ_COLS == 0, "a 32-column TMEM load covers whole chunks");
 };
 
 // Work item number w: (head bh, key block n).  Causal: the heaviest key
@@ -564,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int m = m0 + i;
 #pragma unroll 1
-                for (int c4 = 0; c4 < D / 32; ++c4, ++chunk) {
+                for (int c4 = 0; c4 < D / 32; ++c4) {
                     uint32_t u[32];
                     tmem_ld32(dq_tm + 32 * c4, u);
                     if (c4 == D / 32 - 1) {
@@ -572,24 +579,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_before();
                         mbar_arrive(bar(C::B_DQFREE));
                     }
-                    const int stg = chunk % NSTG;
-                    const uint32_t sbuf = sbase + C::STG_OFF + stg * C::STG_BYTES;
-                    // the reduce (or, right after the epilogue, the dV_n / dK_n
-                    // stores) that last read this staging buffer has finished reading
-                    if (leader && after_epilogue && c4 == 0)
-                        bulk_wait_group_read<0>();
-                    else if (leader && chunk >= NSTG)
-                        bulk_wait_group_read<NSTG - 1>();
-                    named_bar_sync(3, 128);
 #pragma unroll
-                    for (int k8 = 0; k8 < 8; ++k8)
-                        st_shared_v4(sbuf + r * 128 + (((k8 ^ (r & 7)) & 7) << 4), u[4 * k8], u[4 * k8 + 1],
-                                     u[4 * k8 + 2], u[4 * k8 + 3]);
-                    fence_proxy_async_smem();
-                    named_bar_sync(3, 128);
-                    if (leader) {
-                        tma_reduce_add_3d(&tm_dqacc, sbuf, 32 * c4, m * kBlk, bh);
-                        bulk_commit_group();
+                    for (int hh = 0; hh < 32 / C::DQ_COLS; ++hh, ++chunk) {
+                        const int stg = chunk % NSTG;
+                        const uint32_t sbuf = sbase + C::STG_OFF + stg * C::STG_BYTES;
+                        // the reduce (or, right after the epilogue, the dV_n / dK_n
+                        // stores) that last read this staging buffer has finished reading
+                        if (leader && after_epilogue && c4 == 0 && hh == 0)
+                            bulk_wait_group_read<0>();
+                        else if (leader && chunk >= NSTG)
+                            bulk_wait_group_read<NSTG - 1>();
+                        named_bar_sync(3, 128);
+                        if constexpr (C::DQ_COLS == 32) {
+                            // 128-byte rows, 16-byte chunk k at k ^ (r % 8)
+#pragma unroll
+                            for (int k8 = 0; k8 < 8; ++k8)
+                                st_shared_v4(sbuf + r * 128 + (((k8 ^ (r & 7)) & 7) << 4), u[4 * k8], u[4 * k8 + 1],
+                                             u[4 * k8 + 2], u[4 * k8 + 3]);
+                        } else {
+                            // 64-byte rows, 16-byte chunk k at k ^ ((r / 2) % 4)
+#pragma unroll
+                            for (int k4 = 0; k4 < 4; ++k4)
+                                st_shared_v4(sbuf + r * 64 + (((k4 ^ (r >> 1)) & 3) << 4), u[16 * hh + 4 * k4],
+                                             u[16 * hh + 4 * k4 + 1], u[16 * hh + 4 * k4 + 2], u[16 * hh + 4 * k4 + 3]);
+                        }
+                        fence_proxy_async_smem();
+                        named_bar_sync(3, 128);
+                        if (leader) {
+                            tma_reduce_add_3d(&tm_dqacc, sbuf, 32 * c4 + C::DQ_COLS * hh, m * kBlk, bh);
+                            bulk_commit_group();
+                        }
                     }
                 }
             }
