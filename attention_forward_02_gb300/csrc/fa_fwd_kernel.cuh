@@ -537,7 +537,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // than kRescaleLog2 (rare) sends the warp down the redo path.
                 float alpha = 1.f;
                 float rsum;
-                if (j == 0) {
+                if constexpr (EARLY_S) {
+                    // S_h,j is in registers: let the next S_h product in now, so
+                    // that it runs during this tile's exponentials.  The row max
+                    // comes first, so no tile is ever redone from S.
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_SFREE + h));
+                    const float mt = row_max(s);
+                    if (j == 0) {
+                        m_ref = mt;
+                        alpha = 0.f;
+                    } else {
+                        const bool grow = (mt - m_ref) * scale_log2 > kRescaleLog2;
+                        if (__any_sync(0xffffffffu, grow) && grow) {
+                            alpha = ex2_approx((m_ref - mt) * scale_log2);
+                            m_ref = mt;
+                        }
+                    }
+                    rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
+                                  : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
+                } else if (j == 0) {
                     m_ref = row_max(s);
                     alpha = 0.f;
                     rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
@@ -562,9 +581,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 l = l * alpha + rsum;
                 if constexpr (EARLY_S) {
-                    // S_h,j is no longer needed: let the next S_h product in
-                    tc_fence_before();
-                    mbar_arrive(bar(C::B_SFREE + h));
                     // P_h,j-1 V_{j-1} must have read P_h before it is overwritten
                     // (and O_h must be complete before a rescale below).  For
                     // j = 0 the previous item's last product has completed: this
