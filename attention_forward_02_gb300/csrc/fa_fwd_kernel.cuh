@@ -90,19 +90,22 @@ template <int D>
 struct KCfg {
     static_assert(D == 32 || D == 64 || D == 96 || D == 128, "head dims 32, 64, 96, 128");
     static constexpr int TILE = 128 * col_blocks<D>() * 128;  // bytes of one [128, D] 16-bit tile
-    // D <= 64: a 6-slot K/V ring and O staging tiles of their own, so the next
-    // item's Q can land while this item's output is stored.  D > 64: a 4-slot
-    // ring; O is staged in the sub-tile's Q tile, which the next item's Q then
-    // waits for (its items are long, so that wait matters little).
+    // D <= 64: a 6-slot K/V ring, O staging tiles of their own and two Q
+    // buffers per sub-tile, so that the next item's Q lands while this item
+    // still runs and its first S product can follow this item's last S.
+    // D > 64: a 4-slot ring; O is staged in the sub-tile's only Q tile, which
+    // the next item's Q then waits for (its items are long, so that wait
+    // matters little).
     static constexpr bool STAGE_IN_Q = D > 64;
+    static constexpr int QBUF = STAGE_IN_Q ? 1 : 2;
     static constexpr int SLOTS = D <= 64 ? 6 : 4;
-    static constexpr int Q_OFF = 0;                      // Q0, Q1
-    static constexpr int KV_OFF = Q_OFF + 2 * TILE;      // K/V ring
+    static constexpr int Q_OFF = 0;                      // Q tile (h, buffer b) at h + 2 b
+    static constexpr int KV_OFF = Q_OFF + 2 * QBUF * TILE;  // K/V ring
     static constexpr int OST_OFF = STAGE_IN_Q ? Q_OFF : KV_OFF + SLOTS * TILE;  // O staging
     static constexpr int BAR_OFF = KV_OFF + SLOTS * TILE + (STAGE_IN_Q ? 0 : 2 * TILE);
-    static constexpr int B_QFULL = 0;                    // two
-    static constexpr int B_QEMPTY = B_QFULL + 2;         // two
-    static constexpr int B_KVFULL = B_QEMPTY + 2;
+    static constexpr int B_QFULL = 0;                    // 2 QBUF, (h, b) at h + 2 b
+    static constexpr int B_QEMPTY = B_QFULL + 2 * QBUF;  // 2 QBUF
+    static constexpr int B_KVFULL = B_QEMPTY + 2 * QBUF;
     static constexpr int B_KVEMPTY = B_KVFULL + SLOTS;
     static constexpr int B_SFULL = B_KVEMPTY + SLOTS;  // two
     static constexpr int B_PFULL = B_SFULL + 2;        // two
@@ -239,11 +242,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(bar(C::B_KVFULL + s), 1);
             mbar_init(bar(C::B_KVEMPTY + s), NUM_ISSUERS);  // one release per MMA issuer
         }
-        for (int h = 0; h < 2; ++h) {
-            mbar_init(bar(C::B_QFULL + h), 1);
+        for (int q = 0; q < 2 * C::QBUF; ++q) {
+            mbar_init(bar(C::B_QFULL + q), 1);
             // released by the products that read Q_h (one commit) and, when O
             // is staged in Q_h, by the epilogue's stores (128 arrivals)
-            mbar_init(bar(C::B_QEMPTY + h), 1 + (C::STAGE_IN_Q ? 4 * 32 : 0));
+            mbar_init(bar(C::B_QEMPTY + q), 1 + (C::STAGE_IN_Q ? 4 * 32 : 0));
+        }
+        for (int h = 0; h < 2; ++h) {
             mbar_init(bar(C::B_SFULL + h), 1);
             mbar_init(bar(C::B_PFULL + h), 4 * 32);
             mbar_init(bar(C::B_OFINAL + h), 1);
@@ -282,14 +287,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     break;
                 int bh, qb;
                 item_coords<CAUSAL>(w, BH, num_q_blocks, bh, qb);
+                // Q buffer it % QBUF, used for the (it / QBUF)-th time
+                const int qt0 = 2 * (it % C::QBUF), use = it / C::QBUF;
                 for (int h = 0; ok && h < 2; ++h) {
-                    // Q_h of the previous item: every product that read it is done
-                    if (it > 0 && !(ok = wait_bounded(bar(C::B_QEMPTY + h), (it - 1) & 1, abort_flag)))
+                    // Q_h of the item that last used this buffer: every product
+                    // that read it is done
+                    if (use > 0 && !(ok = wait_bounded(bar(C::B_QEMPTY + qt0 + h), (use - 1) & 1, abort_flag)))
                         break;
-                    mbar_arrive_expect_tx(bar(C::B_QFULL + h), C::TILE);
+                    mbar_arrive_expect_tx(bar(C::B_QFULL + qt0 + h), C::TILE);
                     for (int b = 0; b < col_blocks<D>(); ++b)
-                        tma_load_3d(sbase + C::Q_OFF + h * C::TILE + b * kSwAtomBytes, &tm_q,
-                                    bar(C::B_QFULL + h), b * 64, qb * kBM + h * kSubM, bh, pol_q);
+                        tma_load_3d(sbase + C::Q_OFF + (qt0 + h) * C::TILE + b * kSwAtomBytes, &tm_q,
+                                    bar(C::B_QFULL + qt0 + h), b * 64, qb * kBM + h * kSubM, bh, pol_q);
                 }
                 if (!ok)
                     break;
@@ -308,9 +316,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             // Wait for every copy this thread issued (immediate on the normal
             // path, where each one was consumed).
-            for (int h = 0; h < 2; ++h)
-                if (items > 0)
-                    drain_bounded(bar(C::B_QFULL + h), (items - 1) & 1);
+            for (int q = 0; q < 2 * C::QBUF; ++q) {
+                const int b = q / 2;                                 // buffer of Q tile q
+                const int uses = (items - b + C::QBUF - 1) / C::QBUF;  // items that loaded it
+                if (items > b)
+                    drain_bounded(bar(C::B_QFULL + q), (uses - 1) & 1);
+            }
             for (int s = 0; s < SLOTS; ++s)
                 if (L > s)
                     drain_bounded(bar(C::B_KVFULL + s), ((L - 1 - s) / SLOTS) & 1);
@@ -338,12 +349,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const uint64_t desc_v0 = make_sdesc_sw128(sbase + C::KV_OFF, kSwAtomBytes, 1024);
             const uint64_t desc_q0 = make_sdesc_sw128(sbase + C::Q_OFF, 16, 1024);
             int Lb = 0;              // ring index of the current item's K_0
+            int qt0 = 0;             // Q tile of the current item's sub-tile 0
             // key tiles of sub-tile 0 / 1 in earlier items (scalars, not an
             // array: a runtime-indexed array would live in local memory)
             int done0 = 0, done1 = 0;
             auto issue_s = [&](int h, int j) {
                 const uint64_t kd = desc_k0 + static_cast<uint32_t>((slot_of(Lb + 2 * j) * C::TILE) >> 4);
-                const uint64_t qd = desc_q0 + static_cast<uint32_t>((h * C::TILE) >> 4);
+                const uint64_t qd = desc_q0 + static_cast<uint32_t>(((qt0 + h) * C::TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS_QK; ++kk) {
                     const uint32_t koff = static_cast<uint32_t>(((kk >> 2) * kSwAtomBytes + (kk & 3) * 32) >> 4);
@@ -394,8 +406,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int nk0 = nk_sub(qb, 0), nk1 = nk_sub(qb, 1);
                 auto nk_of = [&](int h) { return h == 0 ? nk0 : nk1; };
                 auto done_of = [&](int h) { return h == 0 ? done0 : done1; };
+                qt0 = 2 * (it % C::QBUF);
                 for (int h = h_lo; ok && h < h_hi; ++h) {
-                    ok = wait_bounded(bar(C::B_QFULL + h), it & 1, abort_flag);
+                    ok = wait_bounded(bar(C::B_QFULL + qt0 + h), (it / C::QBUF) & 1, abort_flag);
                     // early-S: S_h,0 overwrites S_h, which the previous item's
                     // last softmax step must have finished reading
                     if (ok && EARLY_S && it > 0)
@@ -482,7 +495,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     break;
                 // every product reading Q_h of this item has been issued
                 for (int h = h_lo; h < h_hi; ++h)
-                    umma_commit(bar(C::B_QEMPTY + h));
+                    umma_commit(bar(C::B_QEMPTY + qt0 + h));
                 done0 += nk0;
                 done1 += nk1;
                 Lb += 2 * nk1;
