@@ -59,9 +59,12 @@ constexpr int kBN = 128;            // keys per K/V tile
 constexpr int kNumThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-constexpr uint32_t kRegsSoftmax = 200;
-constexpr uint32_t kRegsControl = 96;
+constexpr uint32_t kRegsSoftmax = 216;  // d <= 64 (d > 64: 200, its single issuer needs the rest)
+constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsSoftmaxWide = 200;
+constexpr uint32_t kRegsControlWide = 96;
 static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= 384 * 168, "register split");
+static_assert(256 * kRegsSoftmaxWide + 128 * kRegsControlWide <= 384 * 168, "register split");
 // TMEM columns: S0 @ 0, S1 @ 128, O0 @ 256, O1 @ 256 + D.  P_h (16-bit, two
 // per column) takes 64 columns: for D <= 64 the spare columns 256 + 2D + 64 h,
 // for D > 64 the first half of S_h (the next S_h product is issued after the
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp >= kMmaWarp) {
-      reg_dealloc<kRegsControl>();
+      reg_dealloc<(D <= 64 ? kRegsControl : kRegsControlWide)>();
       if (warp == kTmaWarp && lane == 0) {
             // ---------------- producer: per work item Q0, Q1, then K_0, V_0, K_1, V_1, ... ----------------
             tma_prefetch_desc(&tm_q);
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             drain_bounded(bar(C::B_DRAIN + me), 0);
       }
     } else {
-        reg_alloc<kRegsSoftmax>();
+        reg_alloc<(D <= 64 ? kRegsSoftmax : kRegsSoftmaxWide)>();
         // ---------------- softmax warpgroup h (warps 4h .. 4h+3) ----------------
         const int h = warp >> 2;
         const int r = threadIdx.x & 127;  // row within the sub-tile == TMEM lane
