@@ -547,10 +547,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const bool masked = __any_sync(0xffffffffu, limit < kBN);
                 if (masked)
                     mask_tail(s, limit);
-                // Tile 0 sets the reference max from its own row max.  Later tiles
-                // exponentiate against the current reference while their row max
-                // is taken; only a row max that outgrows the reference by more
-                // than kRescaleLog2 (rare) sends the warp down the redo path.
+                // Tile 0 sets the reference max from its own row max; the reference
+                // moves only when a row max outgrows it by more than kRescaleLog2
+                // (rare).  D <= 64 takes the row max before the exponentials; D >
+                // 64 exponentiates against the current reference while the row max
+                // is taken, and redoes the tile from S when the reference moves.
                 float alpha = 1.f;
                 float rsum;
                 if constexpr (EARLY_S) {
