@@ -59,7 +59,7 @@ constexpr int kBN = 128;            // keys per K/V tile
 constexpr int kNumThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-constexpr uint32_t kRegsSoftmax = 216;  // d <= 64 (d > 64: 200, its single issuer needs the rest)
+constexpr uint32_t kRegsSoftmax = 216;  // d <= 64, non-causal (otherwise 200: measured faster there)
 constexpr uint32_t kRegsControl = 72;
 constexpr uint32_t kRegsSoftmaxWide = 200;
 constexpr uint32_t kRegsControlWide = 96;
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp >= kMmaWarp) {
-      reg_dealloc<(D <= 64 ? kRegsControl : kRegsControlWide)>();
+      reg_dealloc<((D <= 64 && !CAUSAL) ? kRegsControl : kRegsControlWide)>();
       if (warp == kTmaWarp && lane == 0) {
             // ---------------- producer: per work item Q0, Q1, then K_0, V_0, K_1, V_1, ... ----------------
             tma_prefetch_desc(&tm_q);
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             drain_bounded(bar(C::B_DRAIN + me), 0);
       }
     } else {
-        reg_alloc<(D <= 64 ? kRegsSoftmax : kRegsSoftmaxWide)>();
+        reg_alloc<((D <= 64 && !CAUSAL) ? kRegsSoftmax : kRegsSoftmaxWide)>();
         // ---------------- softmax warpgroup h (warps 4h .. 4h+3) ----------------
         const int h = warp >> 2;
         const int r = threadIdx.x & 127;  // row within the sub-tile == TMEM lane
