@@ -72,6 +72,12 @@ def parse_args():
                     help="target total host seconds of the --impl reference run")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the d=128 and long-context target workloads in the forward line")
+    ap.add_argument("--no-fa1-ratio", action="store_true",
+                    help="skip the FA2 / FA1 timing table in the forward line")
+    ap.add_argument("--target-steps", type=int, default=5,
+                    help="timed steps per variant of each target workload")
     return ap.parse_args()
 
 
@@ -173,9 +179,16 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return self.summary(*(self.t_load or (0, float("inf"))))
+
+    def summary(self, t0, t1):
+        """Median SM clock, max clock / power and the throttle reasons seen
+        in the samples taken between wall-clock times t0 and t1."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        t0, t1 = self.t_load or (0, float("inf"))
         for ts, line in self.lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 10:
@@ -487,13 +500,21 @@ def main():
         e2e = run_e2e(run, torch, q, k, v, meta, variants, dev, stream, scale, step_flops,
                       max(3, min(K, 50)), dist)
 
-    clocks = sampler.stop()
     peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    targets = None
+    if not args.no_targets and args.kernel == "fa2":
+        targets = time_targets(torch, fa, dev, stream, flush, peak, args.target_steps, sampler,
+                               [w for w in ("d128", "long") if w != args.workload])
+    fa1_ratio = None
+    if not args.no_fa1_ratio and args.kernel == "fa2":
+        fa1_ratio = time_fa2_vs_fa1(torch, fa, dev, stream, flush, args.target_steps)
+
+    clocks = sampler.stop()
     dom = variants.index(False) if False in variants else 0  # the non-causal launch
     dom_causal = variants[dom]
     dom_ms = statistics.mean(per_kernel_ms[dom])
     achieved = flops_of(meta, dom_causal) / (dom_ms / 1e3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     src_hash = kernel_source_hash(args.kernel)
     traffic, traffic_src = recorded_traffic(args.workload, src_hash, args.kernel)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -534,9 +555,108 @@ def main():
                 "dtype": meta["dtype"], "data": "synthetic", "config": config,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": K * nv * 1, "wall_s_timed": t_wall}
+        if targets is not None:
+            line["targets"] = targets
+        if fa1_ratio is not None:
+            line["fa2_vs_fa1"] = fa1_ratio
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def time_launches(torch, run_one, stream, flush, steps, warmup=3):
+    """Mean device time (ms) of run_one() over `steps` launches, each
+    bracketed by CUDA events on the launching stream, with L2 flushed before
+    every launch outside the timed bracket."""
+    for _ in range(warmup):
+        flush.zero_()
+        run_one()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        run_one()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def time_targets(torch, fa, dev, stream, flush, peak, steps, sampler, names):
+    """The other workloads the >= 60 % target names (d=128 B=2 H=16 N=8192
+    bf16 and the long context B=1 H=8 N=65536 d=128 fp16), both variants,
+    timed like the headline: CUDA events per launch, L2 flushed between
+    launches outside the events."""
+    from attention_forward_02_gb300 import inputs
+    out = {}
+    for name in names:
+        q, k, v, meta = inputs.make_workload(name)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        del q, k, v
+        o = torch.empty_like(qd)
+        lse = torch.empty((meta["B"], meta["H"], meta["N"]), dtype=torch.float32, device=dev)
+        scale = meta["d"] ** -0.5
+        t0 = time.time()
+        res = {"config": "%s B=%d H=%d N=%d d=%d %s" % (name, meta["B"], meta["H"], meta["N"],
+                                                         meta["d"], meta["dtype"]),
+               "steps": steps}
+        for causal in (False, True):
+            ms = time_launches(torch, lambda: fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=scale,
+                                                        causal=causal, stream=stream),
+                               stream, flush, steps)
+            tf = flops_of(meta, causal) / (ms / 1e3) / 1e12
+            res["causal" if causal else "noncausal"] = {
+                "tflops": tf, "frac": tf / peak, "launch_ms": ms,
+                "algorithmic_flops_per_launch": flops_of(meta, causal)}
+        st = fa.fa_last_device_status(stream.cuda_stream)
+        if st != 0:
+            raise SystemExit("device status after %s: %s" % (name, fa.fa_status_str(st)))
+        res["clocks"] = sampler.summary(t0, time.time())
+        res["peak"] = peak
+        out[name] = res
+        del qd, kd, vd, o, lse
+        torch.cuda.empty_cache()
+    return out
+
+
+# The pages' FA2 / FA1 ratios on an RTX 5090, each kernel tuned, [4, 32, 2048, 64]
+# fp16 ("Triton으로 FlashAttention 1·2 forward 구현하기", section "기준 shape").
+PAGE_FA2_FA1 = {"noncausal": 2.16, "causal": 1.79}
+
+
+def time_fa2_vs_fa1(torch, fa, dev, stream, flush, steps):
+    """FA2 (fa_fwd) and the FA1-structured loop nest (fa1_fwd) timed in the
+    same process on the page's shape [B, 32, 2048, 64] fp16, B in {1, 2, 4, 8},
+    both variants; ratio = FA1 time / FA2 time."""
+    from attention_forward_02_gb300 import inputs
+    rows = []
+    for B in (1, 2, 4, 8):
+        q, k, v, meta = inputs.make_workload("sweep_b%d" % B)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        o = torch.empty_like(qd)
+        lse = torch.empty((B, 32, 2048), dtype=torch.float32, device=dev)
+        ws = torch.empty(fa.fa1_fwd_workspace_size(B, 32, 2048, 64), dtype=torch.uint8, device=dev)
+        row = {"B": B}
+        for causal in (False, True):
+            t2 = time_launches(torch, lambda: fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=0.125,
+                                                        causal=causal, stream=stream),
+                               stream, flush, steps)
+            t1 = time_launches(torch, lambda: fa.fa1_fwd(qd, kd, vd, o=o, lse=lse, scale=0.125,
+                                                         causal=causal, workspace=ws, stream=stream),
+                               stream, flush, steps)
+            fl = flops_of(meta, causal)
+            row["causal" if causal else "noncausal"] = {
+                "fa2_ms": t2, "fa1_ms": t1, "ratio": t1 / t2,
+                "fa2_tflops": fl / (t2 / 1e3) / 1e12, "fa1_tflops": fl / (t1 / 1e3) / 1e12}
+        st = fa.fa_last_device_status(stream.cuda_stream)
+        if st != 0:
+            raise SystemExit("device status after the FA1 comparison: %s" % fa.fa_status_str(st))
+        rows.append(row)
+        del qd, kd, vd, o, lse, ws
+        torch.cuda.empty_cache()
+    return {"shape": "[B, 32, 2048, 64] fp16, scale 1/8", "ratio": "fa1_ms / fa2_ms",
+            "rows": rows, "page_ratio_B4_rtx5090": PAGE_FA2_FA1}
 
 
 def pipelined_e2e(torch, dev, steps, h2d, compute, d2h):

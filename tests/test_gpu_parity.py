@@ -1,15 +1,16 @@
 """CUDA path vs the fp64 oracle through the C ABI, on seeded inputs.
 
 Small shapes are compared element by element in full (several tiles and a
-ragged tail); the full-size workloads, in the launch configuration the bench
-times, are compared on seeded row samples plus the tile-edge rows."""
+ragged tail).  The full-size workloads, in the launch configuration the bench
+times, are compared element by element too, except the long-context workload
+(512 seeded rows per head)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from attention_forward_02_gb300 import inputs
-from parity_util import check_full, check_rows, edge_rows, run_gpu
+from parity_util import check_full, check_rows, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -54,12 +55,11 @@ def test_head_dims_32_96_full(orc, dtype, d, causal, N):
 
 @pytest.mark.parametrize("name", ["hd32", "hd96", "ragged"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_head_dim_workloads_sampled(orc, name, causal):
+def test_head_dim_workloads_whole_tensor(orc, name, causal):
     q, k, v, meta = inputs.make_workload(name)
-    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
+    d = meta["d"]
     o, lse = run_gpu(q, k, v, d ** -0.5, causal)
-    rows = edge_rows(B, H, N, inputs.sample_rows(B, H, N, 8, 4242))
-    check_rows(orc, q, k, v, d ** -0.5, causal, o, lse, rows, "%s causal=%s" % (name, causal))
+    check_full(orc, q, k, v, d ** -0.5, causal, o, lse, "%s causal=%s (whole tensor)" % (name, causal))
 
 
 @pytest.mark.parametrize("d,dtype", [(64, "fp16"), (128, "bf16")])
@@ -136,22 +136,28 @@ def test_status_errors_on_device(orc):
 
 
 # ---------------------------------------------------------------------------
-# Full-size workloads (bench launch configuration), sampled rows
+# Full-size workloads in the launch configuration the bench times, compared
+# element by element over all of O and LSE (the persistent scheduler deals
+# several work items to every CTA at these sizes).  Only the long-context
+# workload is compared on a row sample (512 seeded rows per head).
 
-FULL = [("base", 1.0, 64), ("sweep_b1", 1.0, 32), ("sweep_b2", 1.0, 32), ("sweep_b4", 1.0, 16),
-        ("sweep_b8", 1.0, 8), ("sweep_b4", 8.0, 16), ("d128", 1.0, 128)]
+FULL = [("base", 1.0), ("sweep_b1", 1.0), ("sweep_b2", 1.0), ("sweep_b4", 1.0),
+        ("sweep_b8", 1.0), ("sweep_b4", 8.0), ("d128", 1.0)]
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("name,q_scale,per_head", FULL, ids=["%s_q%g" % (n, s) for n, s, _ in FULL])
-def test_full_size_sampled(orc, name, q_scale, per_head, causal):
+@pytest.mark.parametrize("name,q_scale", FULL, ids=["%s_q%g" % (n, s) for n, s in FULL])
+def test_full_size_whole_tensor(orc, name, q_scale, causal):
     q, k, v, meta = inputs.make_workload(name, q_scale=q_scale)
-    B, H, N, d = meta["B"], meta["H"], meta["N"], meta["d"]
-    scale = d ** -0.5
+    scale = meta["d"] ** -0.5
     o, lse = run_gpu(q, k, v, scale, causal)
-    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
-    rows = edge_rows(B, H, N, inputs.sample_rows(B, H, N, per_head, 7000 + B))
-    check_rows(orc, q, k, v, scale, causal, o, lse, rows, "%s causal=%s" % (name, causal))
+    res = check_full(orc, q, k, v, scale, causal, o.cpu(), lse.cpu(),
+                     "%s q_scale=%g causal=%s (whole tensor)" % (name, q_scale, causal))
+    # the benchmark spec's fixed bound, reported for every config (asserted for fp16
+    # by check_full; bf16 is held to the derived element-wise bound)
+    print("%s q%g causal=%s: max|dO| %.3g (fixed bound %.3g, %.6f of elements within it), "
+          "max|dLSE| %.3g" % (name, q_scale, causal, res["o_max_err"], res["o_fixed_bound"],
+                               res["frac_within_fixed"], res["lse_max_err"]))
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -2,14 +2,15 @@
 cudaMalloc themselves (for example code inside a host framework that only hands
 it fixed input and output buffers).  It keeps its scratch in a fixed array in
 the library, so this test calls it straight through the C ABI and compares it
-with fa1_fwd, which takes a caller workspace, on two calls in a row with
-different inputs (the second call must not be affected by what the first one
-left in the shared array).  Collected last on purpose."""
+with fa1_fwd, which takes a caller workspace, and with the fp64 oracle, on two
+calls in a row with different inputs (the second call must not be affected by
+what the first one left in the shared array).  Collected last on purpose."""
 import pytest
 import torch
 
+import oracle
 from attention_forward_02_gb300 import inputs
-from parity_util import LSE_TOL, O_TOL_REL_VMAX
+from parity_util import LSE_TOL, O_TOL_REL_VMAX, check_full
 
 pytestmark = pytest.mark.gpu
 
@@ -28,6 +29,7 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
         pytest.skip("no CUDA device")
     import attention_forward_02_gb300 as fa
     dev = torch.device("cuda:0")
+    orc = oracle.get()
     cases = [((1, 2, 700, 64, "fp16", (91, 92, 93)), True),
              ((2, 3, 389, 128, "bf16", (94, 95, 96)), False)]
     for (B, H, N, d, dtype, seeds), causal in cases:
@@ -40,6 +42,9 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
         vmax = float(v.abs().max())
         assert float((o.double() - o_ref.double()).abs().max()) <= O_TOL_REL_VMAX * vmax
         assert float((lse.double() - lse_ref.double()).abs().max()) <= LSE_TOL
+        # and against the oracle itself, element by element
+        check_full(orc, q.cpu(), k.cpu(), v.cpu(), d ** -0.5, causal, o.cpu(), lse.cpu(),
+                   "fa1_fwd_noalloc B%dH%dN%d d=%d %s causal=%s" % (B, H, N, d, dtype, causal))
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
