@@ -13,13 +13,14 @@ without the built library, or off a CUDA device, calls raise ``FAError``.
 from ._lib import (FA_BF16, FA_FP16, FAError, fa1_fwd_raw, fa1_fwd_workspace_size,
                    fa_abi_version, fa_bwd_raw, fa_bwd_workspace_size, fa_decode_raw,
                    fa_decode_workspace_size, fa_fwd_raw, fa_last_device_status,
-                   fa_selftest_wait_timeout, fa_status_str, lib_path, load)
+                   fa_selftest_bounds_check, fa_selftest_wait_timeout, fa_status_str, lib_path,
+                   load, load_checked)
 
 __all__ = ["fa_fwd", "fa_fwd_raw", "fa1_fwd", "fa1_fwd_raw", "fa1_fwd_workspace_size",
            "fa_bwd", "fa_bwd_raw", "fa_bwd_workspace_size",
            "fa_decode", "fa_decode_raw", "fa_decode_workspace_size",
-           "fa_last_device_status", "fa_selftest_wait_timeout",
-           "fa_status_str", "fa_abi_version", "FAError", "load", "lib_path"]
+           "fa_last_device_status", "fa_selftest_wait_timeout", "fa_selftest_bounds_check",
+           "fa_status_str", "fa_abi_version", "FAError", "load", "load_checked", "lib_path"]
 
 
 def _dtype_code(t):

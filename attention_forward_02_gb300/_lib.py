@@ -7,7 +7,7 @@ raises ``FAError``.
 import ctypes
 import os
 
-from .build import LIB
+from .build import LIB, LIB_CHECKED
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = 1
@@ -15,15 +15,18 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_MISALIGNED = 3
 FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
+FA_ERR_BOUNDS = 6
 FA_FP16 = 0
 FA_BF16 = 1
 
 # every symbol include/fa.h declares
 EXPORTS = ("fa_fwd", "fa1_fwd_workspace_size", "fa1_fwd", "fa1_fwd_noalloc", "fa_bwd_workspace_size",
            "fa_bwd", "fa_decode_workspace_size", "fa_decode", "fa_last_device_status",
-           "fa_selftest_wait_timeout", "fa_status_str", "fa_abi_version")
+           "fa_selftest_wait_timeout", "fa_selftest_bounds_check", "fa_checked_build",
+           "fa_status_str", "fa_abi_version")
 
 _lib = None
+_lib_checked = None
 
 
 class FAError(RuntimeError):
@@ -35,16 +38,28 @@ class FAError(RuntimeError):
 
 def status_name(status):
     names = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
-             4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+             4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_BOUNDS"}
     return names.get(int(status), "FA_ERR_UNKNOWN(%d)" % int(status))
 
 
 def load(path=None):
     """Load (once) and return the CUDA library; raise if it is not built."""
     global _lib
-    if _lib is not None:
-        return _lib
-    path = path or LIB
+    if _lib is None:
+        _lib = _open(path or LIB)
+    return _lib
+
+
+def load_checked():
+    """Load (once) and return the checked build of the library (the same
+    entry points with device-side address checks; see include/fa.h)."""
+    global _lib_checked
+    if _lib_checked is None:
+        _lib_checked = _open(LIB_CHECKED)
+    return _lib_checked
+
+
+def _open(path):
     if not os.path.exists(path):
         raise FAError(FA_ERR_CUDA, "CUDA library %s is not built; run "
                       "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
@@ -71,11 +86,14 @@ def load(path=None):
     lib.fa_last_device_status.argtypes = [vp]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, vp]
+    lib.fa_selftest_bounds_check.restype = i
+    lib.fa_selftest_bounds_check.argtypes = [vp]
+    lib.fa_checked_build.restype = i
+    lib.fa_checked_build.argtypes = []
     lib.fa_status_str.restype = ctypes.c_char_p
     lib.fa_status_str.argtypes = [i]
     lib.fa_abi_version.restype = i
     lib.fa_abi_version.argtypes = []
-    _lib = lib
     return lib
 
 
@@ -124,6 +142,10 @@ def fa_last_device_status(stream=None):
 
 def fa_selftest_wait_timeout(limit_us, stream=None):
     return load().fa_selftest_wait_timeout(int(limit_us), stream)
+
+
+def fa_selftest_bounds_check(stream=None):
+    return load().fa_selftest_bounds_check(stream)
 
 
 def fa_status_str(status):

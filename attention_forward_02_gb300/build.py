@@ -1,9 +1,11 @@
 """Build the sm_103a CUDA library in-tree (attention_forward_02_gb300/_build/).
 
-Three translation units (forward, backward, decoding) compiled in parallel, one
--gencode (compute_103a -> sm_103a), static cudart, no link against libcuda
-(the TMA encoder is fetched through the runtime's driver entry-point query).
-Compiles in well under a minute.
+Three translation units (forward, backward, decoding), one -gencode
+(compute_103a -> sm_103a), static cudart, no link against libcuda (the TMA
+encoder is fetched through the runtime's driver entry-point query).  The same
+three units are compiled a second time with FA_BOUNDS_CHECK into the checked
+build (libfa_gb300_checked.so, device-side address checks; a test build).  All
+six compile in parallel.
 """
 import os
 import shutil
@@ -17,6 +19,9 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB = os.path.join(OUT_DIR, LIB_NAME)
+# The same sources with the device-side address checks compiled in
+# (FA_BOUNDS_CHECK; see include/fa.h): a test build, never the product path.
+LIB_CHECKED = os.path.join(OUT_DIR, "libfa_gb300_checked.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa1_fwd_kernel.cuh",
                                                   "fa_bwd_kernel.cuh", "fa_decode_kernel.cuh",
@@ -38,12 +43,12 @@ def _flags():
             "-Xcompiler", "-fvisibility=hidden", "-I" + INCLUDE, "-I" + CSRC]
 
 
-def compile_commands(out, verbose_ptxas=False):
+def compile_commands(out, verbose_ptxas=False, checked=False):
     """One nvcc -c per translation unit, then the link of the shared library."""
     objs, compiles = [], []
     for src in SOURCES:
         obj = out + "." + os.path.splitext(os.path.basename(src))[0] + ".o"
-        cmd = [nvcc_path(), *_flags(), "-c", "-o", obj, src]
+        cmd = [nvcc_path(), *_flags(), *(["-DFA_BOUNDS_CHECK"] if checked else []), "-c", "-o", obj, src]
         if verbose_ptxas:
             cmd.insert(1, "-Xptxas=-v")
         objs.append(obj)
@@ -52,22 +57,35 @@ def compile_commands(out, verbose_ptxas=False):
     return compiles, link, objs
 
 
-def build_library(force=False, verbose_ptxas=False):
-    """Compile the library if a source is newer than it; return its path."""
+def _stale(lib):
+    if not os.path.exists(lib):
+        return True
+    t = os.path.getmtime(lib)
+    return any(os.path.getmtime(p) > t for p in DEPS)
+
+
+def build_library(force=False, verbose_ptxas=False, checked=True):
+    """Compile the library (and, with checked=True, its checked build) if a
+    source is newer than it; return the product library's path.  All
+    translation units compile in parallel."""
     os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB):
-        t = os.path.getmtime(LIB)
-        if all(os.path.getmtime(p) <= t for p in DEPS):
-            return LIB
-    tmp = LIB + ".tmp%d" % os.getpid()
-    compiles, link, objs = compile_commands(tmp, verbose_ptxas)
+    jobs = [(LIB, False)] + ([(LIB_CHECKED, True)] if checked else [])
+    jobs = [(lib, chk) for lib, chk in jobs if force or _stale(lib)]
+    if not jobs:
+        return LIB
+    plans = []
+    for lib, chk in jobs:
+        tmp = lib + ".tmp%d" % os.getpid()
+        plans.append((lib, tmp) + compile_commands(tmp, verbose_ptxas and not chk, chk))
+    compiles = [c for _, _, cs, _, _ in plans for c in cs]
     with ThreadPoolExecutor(len(compiles)) as ex:
         for f in [ex.submit(subprocess.run, c, check=True) for c in compiles]:
             f.result()
-    subprocess.run(link, check=True)
-    for o in objs:
-        os.remove(o)
-    os.replace(tmp, LIB)
+    for lib, tmp, _, link, objs in plans:
+        subprocess.run(link, check=True)
+        for o in objs:
+            os.remove(o)
+        os.replace(tmp, lib)
     return LIB
 
 

@@ -220,7 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // all earlier items (the ring slots and barrier phases run on across items).
     int bh = 0, n = 0;
 
-    auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
+    auto bar = [&](int idx) -> uint32_t {
+        FA_CHECK(idx >= 0 && idx < C::NUM_BARS);
+        return sbase + C::BAR_OFF + 8u * idx;
+    };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + C::SLOT_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SLOT_OFF + 4);
 
@@ -352,8 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return static_cast<uint32_t>(((kk >> 2) * kSwAtomBytes + (kk & 3) * 32) >> 4);
             };
             auto mn = [](int kk) -> uint32_t { return static_cast<uint32_t>((kk * 2048) >> 4); };
-            auto tile = [](int slot) -> uint32_t { return static_cast<uint32_t>((slot * C::TILE) >> 4); };
-            auto kvbuf = [](int b) -> uint32_t { return static_cast<uint32_t>((2 * b * C::TILE) >> 4); };
+            auto tile = [](int slot) -> uint32_t {
+                FA_CHECK(slot >= 0 && slot < (QST > DOST ? QST : DOST));
+                return static_cast<uint32_t>((slot * C::TILE) >> 4);
+            };
+            auto kvbuf = [](int b) -> uint32_t {
+                FA_CHECK(b >= 0 && b < KVBUF);
+                return static_cast<uint32_t>((2 * b * C::TILE) >> 4);
+            };
 
             auto issue_s = [&](int s, int b) {  // S^T = K Q^T
 #pragma unroll

@@ -1,5 +1,5 @@
 // fa_common.cuh -- device pieces shared by the forward and backward kernels:
-// the device status word, bounded mbarrier waits, the 16-bit dtype traits and
+// bounded mbarrier waits, the 16-bit dtype traits and
 // the 128B-swizzle tile addressing.
 #pragma once
 
@@ -12,11 +12,6 @@
 #include "sm100_ptx.cuh"
 
 namespace fa {
-
-// Device status word, one per device and translation unit (the host side of
-// each unit reads and clears its own): bit 0 = a bounded wait expired.
-static __device__ unsigned int g_fa_status;
-constexpr unsigned int kStatusTimeout = 1u;
 
 constexpr long long kWaitLimitCycles = 1ll << 31;  // about one second at 2 GHz
 constexpr int kSwAtomBytes = 128 * 128;             // [128 rows x 64 cols] 16-bit swizzle block

@@ -114,17 +114,23 @@ __device__ __forceinline__ void load8(uint32_t addr, float (&f)[8])
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
 {
     float v;
+    if (!smem_ok(addr, 4, 4))
+        return 0.f;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
 {
     uint32_t v;
+    if (!smem_ok(addr, 4, 4))
+        return 0u;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
 {
+    if (!smem_ok(addr, 4, 4))
+        return;
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 

@@ -423,8 +423,10 @@ fa_status_t fa_last_device_status(void *stream)
     if (fa_host::take_bwd_status(&bwd_word) != FA_OK || fa_host::take_decode_status(&dec_word) != FA_OK)
         return FA_ERR_CUDA;
     word |= bwd_word | dec_word;
-    if (word & ~fa::kStatusTimeout)
-        return FA_ERR_CUDA;  // a self-test wait did not behave as required
+    if (word & fa::kStatusSelftest)
+        return FA_ERR_CUDA;  // a self-test did not behave as required
+    if (word & fa::kStatusBounds)
+        return FA_ERR_BOUNDS;
     return (word & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
@@ -444,6 +446,14 @@ fa_status_t fa_selftest_wait_timeout(int limit_us, void *stream)
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status_t fa_selftest_bounds_check(void *stream)
+{
+    fa::fa_selftest_bounds_kernel<<<1, 128, 1024, static_cast<cudaStream_t>(stream)>>>();
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_checked_build(void) { return fa::kBoundsCheck ? 1 : 0; }
+
 const char *fa_status_str(fa_status_t status)
 {
     switch (status) {
@@ -453,6 +463,7 @@ const char *fa_status_str(fa_status_t status)
     case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_BOUNDS: return "FA_ERR_BOUNDS";
     }
     return "FA_ERR_UNKNOWN";
 }

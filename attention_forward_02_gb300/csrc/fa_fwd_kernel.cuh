@@ -236,7 +236,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         return CAUSAL ? min(2 * qb + 1 + h, num_k_tiles) : num_k_tiles;
     };
 
-    auto bar = [&](int idx) -> uint32_t { return sbase + C::BAR_OFF + 8u * idx; };
+    auto bar = [&](int idx) -> uint32_t {
+        FA_CHECK(idx >= 0 && idx < C::NUM_BARS);
+        return sbase + C::BAR_OFF + 8u * idx;
+    };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + C::SLOT_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SLOT_OFF + 4);
 
@@ -308,6 +311,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int nloads = 2 * nk_sub(qb, 1);  // K_j = load 2j, V_j = load 2j + 1
                 for (int Ll = 0; Ll < nloads; ++Ll, ++L) {
                     const int s = L % SLOTS;
+                    FA_CHECK(s >= 0 && s < SLOTS && qt0 + 1 < 2 * C::QBUF);
                     if (L >= SLOTS && !(ok = wait_bounded(bar(C::B_KVEMPTY + s), ((L / SLOTS) - 1) & 1, abort_flag)))
                         break;
                     const CUtensorMap *map = (Ll & 1) ? &tm_v : &tm_k;
@@ -343,7 +347,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int h_hi = NUM_ISSUERS == 2 ? me + 1 : 2;
             constexpr uint32_t idesc_s = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, kBN, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(DTypeTraits<T>::kBF16, kSubM, D, false, true);
-            auto slot_of = [](int L) { return L % SLOTS; };
+            auto slot_of = [](int L) {
+                FA_CHECK(L >= 0);
+                return L % SLOTS;
+            };
             auto par_of = [](int L) { return static_cast<uint32_t>((L / SLOTS) & 1); };
             // Descriptors of the ring's first tile and of Q0: a tile at byte
             // offset x from them is the same descriptor plus x >> 4 (the start
@@ -721,8 +728,30 @@ __global__ void fa_selftest_wait_kernel(long long limit_cycles)
     if (threadIdx.x == 0) {
         const bool ok = wait_bounded(smem_u32(&bar), 0, &abort_flag, limit_cycles);
         if (ok || abort_flag != 1)
-            atomicOr(&g_fa_status, 2u);  // the wait did not behave as required
+            atomicOr(&g_fa_status, kStatusSelftest);  // the wait did not behave as required
     }
+}
+
+// Self-test of the checked build's address checks: asks them about
+// addresses just inside and just outside the shared window (1 KB of dynamic
+// shared memory) and the tensor-memory columns, performing no access.  The
+// outside ones record kStatusBounds; an inside one that fails, or an outside
+// one that passes, records kStatusSelftest.
+__global__ void fa_selftest_bounds_kernel()
+{
+    extern __shared__ uint8_t smem_raw[];
+    if (threadIdx.x != 32)  // warp 1: lane quarter 32..63
+        return;
+    const uint32_t base = smem_u32(smem_raw);
+    const uint32_t end = smem_window_end();
+    bool good = smem_ok<true>(base, 1024, 16) && smem_ok<true>(end - 16, 16, 16) &&
+                tmem_ok<true>((32u << 16) | 480u, 32, true) && tmem_ok<true>(384u, 128, false);
+    good = good && !smem_ok<true>(end - 8, 16, 8);           // runs past the window
+    good = good && !smem_ok<true>(base + 4, 16, 16);         // misaligned
+    good = good && !tmem_ok<true>((32u << 16) | 496u, 32, true);  // past column 511
+    good = good && !tmem_ok<true>(480u, 32, true);           // another warp's lanes
+    if (!good)
+        atomicOr(&g_fa_status, kStatusSelftest);
 }
 
 }  // namespace fa

@@ -16,10 +16,115 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 }
 
 // ---------------------------------------------------------------------------
+// Device status word and the checked build
+//
+// Device status word, one per device and translation unit (the host side of
+// each unit reads and clears its own): bit 0 = a bounded wait expired, bit 1 =
+// the wait self-test misbehaved, bit 2 = an address check of the checked build
+// failed.
+static __device__ unsigned int g_fa_status;
+constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned int kStatusSelftest = 2u;
+constexpr unsigned int kStatusBounds = 4u;
+
+// Checked build (compiled with -DFA_BOUNDS_CHECK, a second library beside the
+// product one).  Every wrapper below that names a shared-memory or tensor-
+// memory address checks it first: shared addresses must lie inside the
+// block's shared window with their alignment, tensor-memory accesses inside
+// the 512 columns (and, for a warp's loads and stores, in that warp's lane
+// quarter), and the footprint of every MMA operand and accumulator inside its
+// memory.  A failed check records kStatusBounds in the status word and skips
+// the access (no trap): the kernel's bounded waits then end the launch, and
+// the host reads FA_ERR_BOUNDS.  In the product build the checks compile away.
+#ifdef FA_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+constexpr uint32_t kTmemColumns = 512;
+
+static __device__ __noinline__ void bounds_fail() { atomicOr(&g_fa_status, kStatusBounds); }
+
+// One past the last shared-memory byte of the block (static + dynamic; the
+// dynamic area follows the static one).
+__device__ __forceinline__ uint32_t smem_window_end()
+{
+    extern __shared__ uint8_t fa_dynamic_smem[];
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    return smem_u32(fa_dynamic_smem) + dyn;
+}
+
+// The check itself (FORCE: evaluated in either build; used by the self-test).
+template <bool FORCE = false>
+__device__ __forceinline__ bool smem_ok(uint32_t addr, uint32_t bytes, uint32_t align)
+{
+    if (!kBoundsCheck && !FORCE)
+        return true;
+    const uint32_t end = smem_window_end();
+    const bool ok = (addr & (align - 1u)) == 0u && addr < end && bytes <= end - addr;
+    if (!ok)
+        bounds_fail();
+    return ok;
+}
+
+// Columns [col, col + ncols) of tensor memory; lane_quarter: the address is
+// used by this warp's tcgen05.ld / st, whose lanes are 32 (warp % 4) + 0..31.
+template <bool FORCE = false>
+__device__ __forceinline__ bool tmem_ok(uint32_t taddr, uint32_t ncols, bool lane_quarter)
+{
+    if (!kBoundsCheck && !FORCE)
+        return true;
+    const uint32_t col = taddr & 0xFFFFu, lanes = taddr >> 16;
+    bool ok = col < kTmemColumns && ncols <= kTmemColumns - col;
+    if (lane_quarter)
+        ok = ok && lanes == 32u * ((threadIdx.x >> 5) & 3u);
+    else
+        ok = ok && lanes == 0u;
+    if (!ok)
+        bounds_fail();
+    return ok;
+}
+
+// Footprint of a 128B-swizzled operand tile named by a shared-memory matrix
+// descriptor: `rows` rows of the M or N dimension (K-major: 8-row groups SBO
+// apart, each inside one aligned 1024-byte block; MN-major: 64-element
+// column blocks LBO apart, one K step = 16 rows of 128 bytes).
+template <bool FORCE = false>
+__device__ __forceinline__ bool sdesc_ok(uint64_t desc, uint32_t rows, bool mn_major)
+{
+    if (!kBoundsCheck && !FORCE)
+        return true;
+    const uint32_t start = static_cast<uint32_t>(desc & 0x3FFFu) << 4;
+    const uint32_t lbo = static_cast<uint32_t>((desc >> 16) & 0x3FFFu) << 4;
+    const uint32_t sbo = static_cast<uint32_t>((desc >> 32) & 0x3FFFu) << 4;
+    if (mn_major)
+        return smem_ok<FORCE>(start, ((rows + 63u) / 64u - 1u) * lbo + 16u * 128u, 128u);
+    const uint32_t base = start & ~1023u;
+    return smem_ok<FORCE>(base, (rows / 8u - 1u) * sbo + 1024u, 1024u);
+}
+
+// Index check of the checked build (ring slots, buffers, barrier numbers):
+// records kStatusBounds when the condition is false.
+#define FA_CHECK(cond)                            \
+    do {                                          \
+        if (::fa::kBoundsCheck && !(cond))        \
+            ::fa::bounds_fail();                  \
+    } while (0)
+
+// Makes a warp-collective decision uniform (every lane skips or none).
+__device__ __forceinline__ bool warp_all(bool v)
+{
+    return kBoundsCheck ? __all_sync(0xffffffffu, v) : v;
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
+    if (!smem_ok(bar, 8, 8))
+        return;
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
@@ -31,18 +136,24 @@ __device__ __forceinline__ void fence_mbar_init()
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
 {
+    if (!smem_ok(bar, 8, 8))
+        return;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
+    if (!smem_ok(bar, 8, 8))
+        return;
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // True once the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
+    if (!smem_ok(bar, 8, 8))
+        return false;
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -65,6 +176,9 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar, int x,
                                             int y, int z, uint64_t policy)
 {
+    // every box here is at least 1 KB and 128-byte aligned
+    if (!smem_ok(dst, 1024, 128) || !smem_ok(bar, 8, 8))
+        return;
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
@@ -76,6 +190,8 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
 // addresses 16-byte aligned), completion counted on an mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
+    if (!smem_ok(dst, bytes, 16) || !smem_ok(bar, 8, 8))
+        return;
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             dst),
@@ -87,6 +203,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 // written), tracked by the issuing thread's bulk async-group.
 __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int x, int y, int z)
 {
+    if (!smem_ok(src, 1024, 128))
+        return;
     asm volatile(
         "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
             reinterpret_cast<uint64_t>(tmap)),
@@ -98,6 +216,8 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int
 // by element, performed in L2 (atomic with respect to other reductions).
 __device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, uint32_t src, int x, int y, int z)
 {
+    if (!smem_ok(src, 1024, 128))
+        return;
     asm volatile(
         "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
             reinterpret_cast<uint64_t>(tmap)),
@@ -242,6 +362,12 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
 __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate)
 {
+    if (kBoundsCheck) {
+        const uint32_t m = ((idesc >> 24) & 0x1Fu) << 4, n = ((idesc >> 17) & 0x3Fu) << 3;
+        if (!(tmem_ok(d_tmem, n, false) && sdesc_ok(adesc, m, (idesc >> 15) & 1u) &&
+              sdesc_ok(bdesc, n, (idesc >> 16) & 1u)))
+            return;
+    }
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
@@ -255,6 +381,13 @@ __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uin
 __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate)
 {
+    if (kBoundsCheck) {
+        const uint32_t n = ((idesc >> 17) & 0x3Fu) << 3;
+        // A: 128 lanes x 16 elements of 16 bits = 8 columns
+        if (!(tmem_ok(d_tmem, n, false) && tmem_ok(a_tmem, 8, false) &&
+              sdesc_ok(bdesc, n, (idesc >> 16) & 1u)))
+            return;
+    }
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
@@ -267,6 +400,8 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 // before the commit has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
+    if (!smem_ok(bar, 8, 8))
+        return;
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      bar)
                  : "memory");
@@ -293,6 +428,12 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 {
+    if (!warp_all(tmem_ok(taddr, 32, true))) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            r[i] = 0;
+        return;
+    }
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -306,6 +447,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 // 64 consecutive columns: two .x32 loads, one wait.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&f)[64])
 {
+    if (!warp_all(tmem_ok(taddr, 64, true))) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            f[i] = 0;
+        return;
+    }
     uint32_t(&r)[64] = reinterpret_cast<uint32_t(&)[64]>(f);
     asm volatile(
         "{\n\t.reg .b32 t;\n\t"
@@ -325,6 +472,12 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&f)[64])
 // 128 consecutive columns: four .x32 loads, one wait.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&f)[128])
 {
+    if (!warp_all(tmem_ok(taddr, 128, true))) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+            f[i] = 0;
+        return;
+    }
     uint32_t(&r)[128] = reinterpret_cast<uint32_t(&)[128]>(f);
     asm volatile(
         "{\n\t.reg .b32 t;\n\t"
@@ -352,6 +505,8 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&f)[128])
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
 {
+    if (!warp_all(tmem_ok(taddr, 16, true)))
+        return;
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
         "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
@@ -362,6 +517,8 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
 {
+    if (!warp_all(tmem_ok(taddr, 32, true)))
+        return;
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
         "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
@@ -373,6 +530,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64])
 {
+    if (!warp_all(tmem_ok(taddr, 64, true)))
+        return;
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], "
         "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
@@ -392,6 +551,8 @@ __device__ __forceinline__ void tmem_wait_st()
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)
 {
+    if (!smem_ok(addr, 16, 16))
+        return;
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
@@ -400,6 +561,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 {
     uint4 v;
+    if (!smem_ok(addr, 16, 16))
+        return make_uint4(0, 0, 0, 0);
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr)

@@ -564,13 +564,22 @@ def main():
         dist.destroy_process_group()
 
 
-def time_launches(torch, run_one, stream, flush, steps, warmup=3):
-    """Mean device time (ms) of run_one() over `steps` launches, each
-    bracketed by CUDA events on the launching stream, with L2 flushed before
-    every launch outside the timed bracket."""
-    for _ in range(warmup):
+def time_launches(torch, run_one, stream, flush, steps, warmup=3, min_seconds=0.0):
+    """Mean device time (ms) of run_one() over `steps` launches (more, up to
+    400, if that many take under min_seconds of device time), each bracketed
+    by CUDA events on the launching stream, with L2 flushed before every
+    launch outside the timed bracket."""
+    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(warmup):
         flush.zero_()
+        if i == warmup - 1:
+            a0.record(stream)
         run_one()
+        if i == warmup - 1:
+            b0.record(stream)
+    torch.cuda.synchronize()
+    est_s = max(a0.elapsed_time(b0), 1e-3) / 1e3
+    steps = max(steps, min(400, int(min_seconds / est_s) + 1))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     torch.cuda.synchronize()
@@ -580,7 +589,7 @@ def time_launches(torch, run_one, stream, flush, steps, warmup=3):
         run_one()
         b.record(stream)
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return statistics.mean(a.elapsed_time(b) for a, b in evs), steps
 
 
 def time_targets(torch, fa, dev, stream, flush, peak, steps, sampler, names):
@@ -599,15 +608,15 @@ def time_targets(torch, fa, dev, stream, flush, peak, steps, sampler, names):
         scale = meta["d"] ** -0.5
         t0 = time.time()
         res = {"config": "%s B=%d H=%d N=%d d=%d %s" % (name, meta["B"], meta["H"], meta["N"],
-                                                         meta["d"], meta["dtype"]),
-               "steps": steps}
+                                                         meta["d"], meta["dtype"])}
         for causal in (False, True):
-            ms = time_launches(torch, lambda: fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=scale,
-                                                        causal=causal, stream=stream),
-                               stream, flush, steps)
+            # at least ~0.3 s of launches per variant, so the clock sampler sees them
+            ms, n = time_launches(torch, lambda: fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=scale,
+                                                           causal=causal, stream=stream),
+                                  stream, flush, steps, min_seconds=0.3)
             tf = flops_of(meta, causal) / (ms / 1e3) / 1e12
             res["causal" if causal else "noncausal"] = {
-                "tflops": tf, "frac": tf / peak, "launch_ms": ms,
+                "tflops": tf, "frac": tf / peak, "launch_ms": ms, "steps": n,
                 "algorithmic_flops_per_launch": flops_of(meta, causal)}
         st = fa.fa_last_device_status(stream.cuda_stream)
         if st != 0:
@@ -639,12 +648,13 @@ def time_fa2_vs_fa1(torch, fa, dev, stream, flush, steps):
         ws = torch.empty(fa.fa1_fwd_workspace_size(B, 32, 2048, 64), dtype=torch.uint8, device=dev)
         row = {"B": B}
         for causal in (False, True):
-            t2 = time_launches(torch, lambda: fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=0.125,
-                                                        causal=causal, stream=stream),
-                               stream, flush, steps)
-            t1 = time_launches(torch, lambda: fa.fa1_fwd(qd, kd, vd, o=o, lse=lse, scale=0.125,
-                                                         causal=causal, workspace=ws, stream=stream),
-                               stream, flush, steps)
+            t2, _ = time_launches(torch, lambda: fa.fa_fwd(qd, kd, vd, o=o, lse=lse, scale=0.125,
+                                                           causal=causal, stream=stream),
+                                  stream, flush, steps)
+            t1, _ = time_launches(torch, lambda: fa.fa1_fwd(qd, kd, vd, o=o, lse=lse, scale=0.125,
+                                                            causal=causal, workspace=ws,
+                                                            stream=stream),
+                                  stream, flush, steps)
             fl = flops_of(meta, causal)
             row["causal" if causal else "noncausal"] = {
                 "fa2_ms": t2, "fa1_ms": t1, "ratio": t1 / t2,

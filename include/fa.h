@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 3
+#define FA_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define FA_API __attribute__((visibility("default")))
@@ -52,8 +52,11 @@ typedef enum {
                                N beyond the grid limit, device not sm_103 */
     FA_ERR_MISALIGNED = 3,  /* q, k, v or o not 16-byte aligned; lse not 4-byte */
     FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or the launch failed */
-    FA_ERR_TIMEOUT = 5      /* a kernel wait gave up (reported by
+    FA_ERR_TIMEOUT = 5,     /* a kernel wait gave up (reported by
                                fa_last_device_status after the stream drained) */
+    FA_ERR_BOUNDS = 6       /* checked build only: a device-side address check
+                               failed and the access was skipped (reported by
+                               fa_last_device_status) */
 } fa_status_t;
 
 /* Element type of Q, K, V and O (all four share it); accumulation is fp32. */
@@ -230,9 +233,22 @@ FA_API fa_status_t fa_decode(const void *q, const void *k, const void *v, void *
 
 /*
  * fa_last_device_status -- synchronise `stream`, read and clear the device
- * status word of the current device.  Returns FA_ERR_TIMEOUT if any kernel
- * launched since the last call gave up on a wait, FA_ERR_CUDA if the stream
- * reports an error, else FA_OK.  Not for use during CUDA graph capture.
+ * status word of the current device.  Returns FA_ERR_BOUNDS if a kernel of
+ * the checked build (below) failed an address check, else FA_ERR_TIMEOUT if
+ * any kernel launched since the last call gave up on a wait, FA_ERR_CUDA if
+ * the stream reports an error, else FA_OK.  Not for use during CUDA graph
+ * capture.
+ *
+ * Checked build.  The same sources compiled with FA_BOUNDS_CHECK give a second
+ * library (libfa_gb300_checked.so) with the same entry points, for testing in
+ * place of a memory checker: before every shared-memory and tensor-memory
+ * access (TMA copies, MMA operands and accumulators, tensor-memory loads and
+ * stores, mbarrier operations, shared loads and stores) its kernels check the
+ * address against the block's shared window and the 512 tensor-memory
+ * columns (and a warp's own lane quarter), and check ring-slot, buffer and
+ * barrier indices.  A failed check skips the access and sets a bit that
+ * fa_last_device_status reports as FA_ERR_BOUNDS; nothing traps.  The product
+ * library compiles the checks away.
  */
 FA_API fa_status_t fa_last_device_status(void *stream);
 
@@ -246,6 +262,22 @@ FA_API fa_status_t fa_last_device_status(void *stream);
  * traps, and the CUDA context stays usable.  Returns FA_OK once launched.
  */
 FA_API fa_status_t fa_selftest_wait_timeout(int limit_us, void *stream);
+
+/*
+ * fa_selftest_bounds_check -- exercises the checked build's address checks
+ * without touching memory.  Launches one small kernel on `stream` that asks
+ * the same check functions about addresses inside and outside the shared
+ * window and the tensor-memory columns, in either build, and performs no
+ * access with them.  The outside ones must fail, which records the
+ * FA_ERR_BOUNDS bit; an inside one that failed records a self-test fault.
+ * fa_last_device_status then returns FA_ERR_BOUNDS (or FA_ERR_CUDA if a check
+ * misbehaved).  Returns FA_OK once launched.  The pages have no counterpart:
+ * this is test support.
+ */
+FA_API fa_status_t fa_selftest_bounds_check(void *stream);
+
+/* 1 if this library was built with the device-side address checks, else 0. */
+FA_API int fa_checked_build(void);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 FA_API const char *fa_status_str(fa_status_t status);

@@ -35,6 +35,15 @@ def test_every_declared_symbol_is_exported(lib):
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
+def test_checked_build_exports_the_same_symbols(lib):
+    """The checked build (device-side address checks) is the same ABI."""
+    chk = _lib.load_checked()
+    for name in declared_functions():
+        assert hasattr(chk, name), name
+    assert chk.fa_checked_build() == 1 and lib.fa_checked_build() == 0
+    assert chk.fa_abi_version() == lib.fa_abi_version()
+
+
 def test_abi_version_matches_header(lib):
     m = re.search(r"#define FA_ABI_VERSION (\d+)", open(HEADER).read())
     assert fa.fa_abi_version() == int(m.group(1))
@@ -42,7 +51,7 @@ def test_abi_version_matches_header(lib):
 
 def test_status_strings(lib):
     names = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
-             "FA_ERR_CUDA", "FA_ERR_TIMEOUT"]
+             "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_BOUNDS"]
     for code, name in enumerate(names):
         assert fa.fa_status_str(code) == name
         assert _lib.status_name(code) == name

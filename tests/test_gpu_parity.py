@@ -153,8 +153,10 @@ def test_full_size_whole_tensor(orc, name, q_scale, causal):
     o, lse = run_gpu(q, k, v, scale, causal)
     res = check_full(orc, q, k, v, scale, causal, o.cpu(), lse.cpu(),
                      "%s q_scale=%g causal=%s (whole tensor)" % (name, q_scale, causal))
-    # the benchmark spec's fixed bound, reported for every config (asserted for fp16
-    # by check_full; bf16 is held to the derived element-wise bound)
+    # The fixed bound max|dO| <= 2e-3 max|V| holds over the whole tensor at
+    # these sizes for bf16 too (check_full asserts it for fp16 and the derived
+    # element-wise bound for bf16, which the short rows of small cases need).
+    assert res["o_max_err"] <= res["o_fixed_bound"], res
     print("%s q%g causal=%s: max|dO| %.3g (fixed bound %.3g, %.6f of elements within it), "
           "max|dLSE| %.3g" % (name, q_scale, causal, res["o_max_err"], res["o_fixed_bound"],
                                res["frac_within_fixed"], res["lse_max_err"]))
