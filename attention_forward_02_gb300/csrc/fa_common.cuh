@@ -66,6 +66,16 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// Warp-wide bounded wait (every lane of the warp calls it, on the same
+// barrier and parity): one try_wait and one vote when the phase has already
+// completed, the bounded loop otherwise.  Every lane gets the same result.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (__builtin_expect(__all_sync(0xffffffffu, mbar_try_wait(bar, parity)), 1))
+        return true;
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag));
+}
+
 // Bounded wait used on the way out (ignores the abort flag: it waits for
 // work this thread itself started).
 __device__ __forceinline__ void drain_bounded(uint32_t bar, uint32_t parity)

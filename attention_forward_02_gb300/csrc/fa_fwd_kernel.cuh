@@ -17,7 +17,10 @@
 //   warpgroup h runs the softmax of tile j, the tensor core runs the other
 //   sub-tile's P V and Q K^T products.
 //   warp 9       TMA producer: Q0, Q1 once; then K_0, V_0, K_1, V_1, ... through
-//                a SLOTS-deep ring of 128B-swizzled shared tiles.
+//                a SLOTS-deep ring of 128B-swizzled shared tiles.  With D <= 64
+//                the softmax warpgroups free the ring slots (K_j once their
+//                S_h,j is complete, V_j once P_h,j V_j is), which keeps those
+//                commits off the MMA issuers; with D > 64 the issuer does.
 //   warps 8, 10  MMA issuers of sub-tiles 0 and 1 (one thread each), per key
 //                tile j: O_h += P_h,j V_j and S_h,j+1 = Q_h K_{j+1}^T
 //                (tcgen05.mma, fp32 accumulators in TMEM).  V is an MN-major
@@ -26,8 +29,8 @@
 //                = TMEM lane t.  It loads S, masks, takes the row max, updates
 //                the reference max, rescales l and O (in TMEM) by alpha, forms
 //                p = 2^(s*c - m*c) with one FMA + ex2, sums l in fp32, rounds P
-//                to the input dtype (into TMEM over S, or into shared memory),
-//                and finally writes O / l and LSE.
+//                to the input dtype (D <= 64: in the same loop) into TMEM, and
+//                finally writes O / l and LSE.
 // The reference max moves only when the row max grows by more than
 // kRescaleLog2 (in log2 units).  O and l always share the same reference, so
 // the final O / l and LSE are unchanged (the same algebra as section 3.6.4:
@@ -177,6 +180,35 @@ __device__ __forceinline__ float exp_tile(float (&s)[kBN], int limit, float c2, 
     return t.x + t.y;
 }
 
+// As exp_tile, but each pair of exponentials is rounded to 16 bits in the
+// same loop (pw[c] = keys 2c, 2c + 1), so the conversions run beside the
+// ex2 work instead of after it; s is left as it was.  Returns the fp32 row sum.
+template <bool MASKED, typename T>
+__device__ __forceinline__ float exp_pack_tile(const float (&s)[kBN], uint32_t (&pw)[kBN / 2], int limit, float c2,
+                                               float neg_mc)
+{
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        acc[i] = make_float2(0.f, 0.f);
+    const float2 cc = make_float2(c2, c2);
+    const float2 nn = make_float2(neg_mc, neg_mc);
+#pragma unroll
+    for (int c = 0; c < kBN; c += 2) {
+        const float2 x = ffma2(make_float2(s[c], s[c + 1]), cc, nn);
+        float e0 = ex2_approx(x.x);
+        float e1 = ex2_approx(x.y);
+        if (MASKED) {
+            e0 = (c < limit) ? e0 : 0.f;
+            e1 = (c + 1 < limit) ? e1 : 0.f;
+        }
+        pw[c >> 1] = DTypeTraits<T>::pack(e0, e1);
+        acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], make_float2(e0, e1));
+    }
+    const float2 t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    return t.x + t.y;
+}
+
 // Work item w (a 256-row Q block of one head) of a launch with BH heads and
 // nqb Q blocks per head.  Non-causal: head-major, so the CTAs working at the
 // same time share few heads' K/V in L2.  Causal: heaviest blocks (highest qb)
@@ -246,7 +278,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; ++s) {
             mbar_init(bar(C::B_KVFULL + s), 1);
-            mbar_init(bar(C::B_KVEMPTY + s), NUM_ISSUERS);  // one release per MMA issuer
+            // released by the two softmax warpgroups (early-S order) or by
+            // each MMA issuer
+            mbar_init(bar(C::B_KVEMPTY + s), EARLY_S ? 2 : NUM_ISSUERS);
         }
         for (int q = 0; q < 2 * C::QBUF; ++q) {
             mbar_init(bar(C::B_QFULL + q), 1);
@@ -340,8 +374,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // gets its own issuer (warps 8 and 10), so one issues while the
             // other waits.  With D = 128 one issuer serves both sub-tiles in a
             // fixed ping-pong order, which keeps each sub-tile's products
-            // together.  Each issuer releases every K/V load once (after its
-            // products read it, or after it lands if it reads none of it).
+            // together, and releases every K/V load once (after its products
+            // read it).  With D = 64 the softmax warpgroups release them.
             const int me = (warp == kMmaWarp) ? 0 : 1;
             const int h_lo = NUM_ISSUERS == 2 ? me : 0;
             const int h_hi = NUM_ISSUERS == 2 ? me + 1 : 2;
@@ -432,30 +466,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     issue_s(h, 0);
                     umma_commit(bar(C::B_SFULL + h));
                 }
-                release(0, true);
+                if constexpr (!EARLY_S)
+                    release(0, true);
                 for (int j = 0; ok && j < nk1; ++j) {
                     if constexpr (EARLY_S) {
                         // next S products first, then this tile's P V products
-                        bool k_used = false;
                         for (int h = h_lo; ok && h < h_hi; ++h) {
                             if (j + 1 >= nk_of(h))
                                 continue;
                             ok = wait_bounded(bar(C::B_SFREE + h), (done_of(h) + j) & 1, abort_flag) &&
-                                 (k_used || wait_load(2 * j + 2));
+                                 wait_load(2 * j + 2);
                             if (!ok)
                                 break;
                             tc_fence_after();
                             issue_s(h, j + 1);
                             umma_commit(bar(C::B_SFULL + h));
-                            k_used = true;
                         }
-                        if (ok && j + 1 < nk1)
-                            ok = release(2 * j + 2, k_used);
-                        bool v_used = false;
                         for (int h = h_lo; ok && h < h_hi; ++h) {
                             if (j >= nk_of(h))
                                 continue;
-                            ok = (v_used || wait_load(2 * j + 1)) &&
+                            ok = wait_load(2 * j + 1) &&
                                  wait_bounded(bar(C::B_PFULL + h), (done_of(h) + j) & 1, abort_flag) &&
                                  (j > 0 || o_free(h, it));
                             if (!ok)
@@ -465,10 +495,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             umma_commit(bar(C::B_OREADY + h));
                             if (j + 1 == nk_of(h))
                                 umma_commit(bar(C::B_OFINAL + h));
-                            v_used = true;
                         }
-                        if (ok)
-                            ok = release(2 * j + 1, v_used);
                     } else {
                         // per sub-tile: P V of this tile, then the next S product
                         bool v_used = false, k_used = false;
@@ -525,6 +552,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint32_t p_tm = tmem + lane_base + tmem_p_col<D>(h);
         const uint32_t stage = sbase + C::OST_OFF + h * C::TILE;
         int done = 0;  // key tiles of this sub-tile in earlier items
+        int Lr = 0;    // ring index of the current item's K_0
+        // Early-S order: one thread per warpgroup frees the K/V ring slots
+        // (both warpgroups must have freed a slot before it is loaded again).
+        const bool rel = EARLY_S && r == 0;
+        auto kv_free = [&](int l) {
+            if (rel)
+                mbar_arrive(bar(C::B_KVEMPTY + (Lr + l) % SLOTS));
+        };
         for (int it = 0;; ++it) {
             const int w = item_of<CAUSAL>(it);
             if (w >= num_items)
@@ -539,10 +574,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             bool ok = true;
             for (int j = 0; j < nkh; ++j) {
                 const uint32_t ph = static_cast<uint32_t>((done + j) & 1);
-                ok = wait_bounded(bar(C::B_SFULL + h), ph, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
+                ok = wait_warp(bar(C::B_SFULL + h), ph, abort_flag);
                 if (!ok)
                     break;
+                kv_free(2 * j);  // S_h,j has read K_j
                 tc_fence_after();
                 float s[kBN];
                 tmem_ld128(s_tm, s);
@@ -561,6 +596,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // is taken, and redoes the tile from S when the reference moves.
                 float alpha = 1.f;
                 float rsum;
+                uint32_t pw[64];  // P_h,j rounded to the input dtype, two per word
                 if constexpr (EARLY_S) {
                     // S_h,j is in registers: let the next S_h product in now, so
                     // that it runs during this tile's exponentials.  The row max
@@ -578,8 +614,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             m_ref = mt;
                         }
                     }
-                    rsum = masked ? exp_tile<true>(s, limit, scale_log2, -m_ref * scale_log2)
-                                  : exp_tile<false>(s, limit, scale_log2, -m_ref * scale_log2);
+                    rsum = masked ? exp_pack_tile<true, T>(s, pw, limit, scale_log2, -m_ref * scale_log2)
+                                  : exp_pack_tile<false, T>(s, pw, limit, scale_log2, -m_ref * scale_log2);
                 } else if (j == 0) {
                     m_ref = row_max(s);
                     alpha = 0.f;
@@ -610,21 +646,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     // j = 0 the previous item's last product has completed: this
                     // warpgroup waited for it before its epilogue.
                     if (j > 0) {
-                        ok = wait_bounded(bar(C::B_OREADY + h), ph ^ 1u, abort_flag);
-                        ok = __all_sync(0xffffffffu, ok);
+                        ok = wait_warp(bar(C::B_OREADY + h), ph ^ 1u, abort_flag);
                         if (!ok)
                             break;
+                        kv_free(2 * j - 1);  // P_h,j-1 V_j-1 has read V_j-1
                         tc_fence_after();
                     }
                 }
-                // P_h,j rounded to the input dtype
-                {
-                    uint32_t pw[64];
+                // P_h,j rounded to the input dtype (early-S order: done above)
+                if constexpr (!EARLY_S) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
                         pw[c] = DTypeTraits<T>::pack(s[2 * c], s[2 * c + 1]);
-                    tmem_st64(p_tm, pw);
                 }
+                tmem_st64(p_tm, pw);
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     // O_h must hold P V up to tile j-1, and P_h,j V_j is not issued
                     // before this warpgroup arrives below.  In the early-S order
@@ -653,11 +688,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // Both named barriers below are reached by all four warps, whatever
             // happened; their OR-reductions give every warp the same decision.
             if (ok) {
-                ok = wait_bounded(bar(C::B_OFINAL + h), it & 1, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
+                ok = wait_warp(bar(C::B_OFINAL + h), it & 1, abort_flag);
             }
             if (ok) {
                 tc_fence_after();
+                if (rel) {
+                    kv_free(2 * nkh - 1);  // the last P V product has read V
+                    // key tiles this sub-tile skips (causal, sub-tile 0): freed
+                    // once they have landed (so that no slot is freed early)
+                    const int nk1 = nk_sub(qb, 1);
+                    for (int ll = 2 * nkh; ok && ll < 2 * nk1; ++ll) {
+                        const int L = Lr + ll;
+                        ok = wait_bounded(bar(C::B_KVFULL + L % SLOTS), static_cast<uint32_t>((L / SLOTS) & 1),
+                                          abort_flag);
+                        if (ok)
+                            kv_free(ll);
+                    }
+                }
                 const float inv_l = 1.f / l;
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -700,6 +747,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (named_bar_or(1 + h, 4 * 32, bad || *abort_flag != 0))
                 break;
             done += nkh;
+            Lr += 2 * nk_sub(qb, 1);
         }
         tc_fence_before();
     }
