@@ -106,27 +106,28 @@ void init_device(int dev, DeviceState &st)
 // Persistent launch: one CTA per SM (TMEM and shared memory allow one), each
 // walking its share of the (batch*head, 256-row Q block) work items.
 template <int D, bool CAUSAL, typename T>
-fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o,
-                   float *lse, int BH, int N, float scale, int num_sms, cudaStream_t stream)
+fa_status_t launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                   void *o, float *lse, int BH, int N, float scale, int num_sms, cudaStream_t stream)
 {
     const int num_q_blocks = (N + fa::kBM - 1) / fa::kBM;
     const long long items = static_cast<long long>(BH) * num_q_blocks;
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
     fa::fa_fwd_kernel<D, CAUSAL, T><<<grid, fa::kNumThreads, fa::KCfg<D>::SMEM_ALLOC, stream>>>(
-        mq, mk, mv, static_cast<T *>(o), lse, N, BH, num_q_blocks, scale, scale_log2);
+        mq, mk, mv, mo, static_cast<T *>(o), lse, N, BH, num_q_blocks, scale, scale_log2);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 // Head-dim and causal dispatch of the FA2 launch.
 template <typename T>
-fa_status_t launch_d(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o, float *lse,
-                     int BH, int N, int d, float scale, int causal, int num_sms, cudaStream_t stream)
+fa_status_t launch_d(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                     void *o, float *lse, int BH, int N, int d, float scale, int causal, int num_sms,
+                     cudaStream_t stream)
 {
 #define FA_LAUNCH_D(DD)                                                                                  \
     if (d == DD)                                                                                         \
-        return causal ? launch<DD, true, T>(mq, mk, mv, o, lse, BH, N, scale, num_sms, stream)           \
-                      : launch<DD, false, T>(mq, mk, mv, o, lse, BH, N, scale, num_sms, stream);
+        return causal ? launch<DD, true, T>(mq, mk, mv, mo, o, lse, BH, N, scale, num_sms, stream)       \
+                      : launch<DD, false, T>(mq, mk, mv, mo, o, lse, BH, N, scale, num_sms, stream);
     FA_LAUNCH_D(32)
     FA_LAUNCH_D(64)
     FA_LAUNCH_D(96)
@@ -335,13 +336,17 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
     if (s != FA_OK || empty)
         return s;
     const int bh = B * H;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     int sms = 0;
     if ((s = prepare(q, k, v, bh, N, d, dtype, &mq, &mk, &mv, &sms)) != FA_OK)
         return s;
+    // O has Q's layout; the epilogue writes it through a map of the same shape
+    EncodeTiledFn enc = nullptr;
+    if ((s = fa_host::encoder(&enc, nullptr)) != FA_OK || (s = encode_qkv_map(enc, &mo, o, bh, N, d, dtype)) != FA_OK)
+        return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    return dtype == FA_FP16 ? launch_d<__half>(mq, mk, mv, o, lse, bh, N, d, scale, causal, sms, cs)
-                            : launch_d<__nv_bfloat16>(mq, mk, mv, o, lse, bh, N, d, scale, causal, sms, cs);
+    return dtype == FA_FP16 ? launch_d<__half>(mq, mk, mv, mo, o, lse, bh, N, d, scale, causal, sms, cs)
+                            : launch_d<__nv_bfloat16>(mq, mk, mv, mo, o, lse, bh, N, d, scale, causal, sms, cs);
 }
 
 size_t fa1_fwd_workspace_size(int B, int H, int N, int d)

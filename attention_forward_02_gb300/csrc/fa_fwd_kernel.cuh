@@ -30,7 +30,8 @@
 //                the reference max, rescales l and O (in TMEM) by alpha, forms
 //                p = 2^(s*c - m*c) with one FMA + ex2, sums l in fp32, rounds P
 //                to the input dtype (D <= 64: in the same loop) into TMEM, and
-//                finally writes O / l and LSE.
+//                finally stages O / l in shared memory (D <= 64: one TMA
+//                tensor store writes it out) and writes LSE.
 // The reference max moves only when the row max grows by more than
 // kRescaleLog2 (in log2 units).  O and l always share the same reference, so
 // the final O / l and LSE are unchanged (the same algebra as section 3.6.4:
@@ -238,8 +239,8 @@ __device__ __forceinline__ int item_of(int it)
 template <int D, bool CAUSAL, typename T>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, T *__restrict__ out,
-                  float *__restrict__ lse, int N, int BH, int num_q_blocks, float scale,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  T *__restrict__ out, float *__restrict__ lse, int N, int BH, int num_q_blocks, float scale,
                   float scale_log2)
 {
     using C = KCfg<D>;
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int q = 0; q < 2 * C::QBUF; ++q) {
             mbar_init(bar(C::B_QFULL + q), 1);
             // released by the products that read Q_h (one commit) and, when O
-            // is staged in Q_h, by the epilogue's stores (128 arrivals)
+            // is staged in Q_h, by the epilogue's copy-out (128 arrivals)
             mbar_init(bar(C::B_QEMPTY + q), 1 + (C::STAGE_IN_Q ? 4 * 32 : 0));
         }
         for (int h = 0; h < 2; ++h) {
@@ -720,6 +721,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                      DTypeTraits<T>::pack(f[6] * inv_l, f[7] * inv_l));
                     }
                 }
+                // the staged tile goes out through the TMA engine (async proxy)
+                fence_proxy_async_smem();
                 // O_h has been read: the next item's first P V product may overwrite it
                 tc_fence_before();
                 mbar_arrive(bar(C::B_OFREE + h));
@@ -727,23 +730,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     lse[static_cast<size_t>(bh) * N + qrow] = m_ref * scale + logf(l);
             }
             const bool bad = named_bar_or(1 + h, 4 * 32, !ok || *abort_flag != 0);
-            if (!bad) {
-                constexpr int CHUNKS_PER_ROW = D / 8;
-                uint8_t *obase = reinterpret_cast<uint8_t *>(out) +
-                                 (static_cast<size_t>(bh) * N + row0) * D * sizeof(T);
-#pragma unroll 4
-                for (int idx = r; idx < kSubM * CHUNKS_PER_ROW; idx += 4 * 32) {
-                    const int row = idx / CHUNKS_PER_ROW;
-                    const int ch = idx % CHUNKS_PER_ROW;
-                    const uint4 val = ld_shared_v4(stage + sw128_offset(row, ch));
-                    if (row0 + row < N)
-                        *reinterpret_cast<uint4 *>(obase + (static_cast<size_t>(row) * D + ch * 8) *
-                                                               sizeof(T)) = val;
+            if constexpr (!C::STAGE_IN_Q) {
+                // one tensor store per 64-column block; rows past N and columns
+                // past D lie outside the tensor and are not written
+                if (r == 0 && !bad) {
+                    for (int b = 0; b < col_blocks<D>(); ++b)
+                        tma_store_3d(&tm_o, stage + b * kSwAtomBytes, b * 64, row0, bh);
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();  // the staging tile has been read
                 }
+            } else {
+                // O staged in Q_h: the warpgroup copies it out itself (16-byte
+                // coalesced stores), which frees Q_h for the next item's Q
+                // sooner than a tensor store that one thread waits for
+                if (!bad) {
+                    constexpr int CHUNKS_PER_ROW = D / 8;
+                    uint8_t *obase = reinterpret_cast<uint8_t *>(out) +
+                                     (static_cast<size_t>(bh) * N + row0) * D * sizeof(T);
+#pragma unroll 4
+                    for (int idx = r; idx < kSubM * CHUNKS_PER_ROW; idx += 4 * 32) {
+                        const int row = idx / CHUNKS_PER_ROW;
+                        const int ch = idx % CHUNKS_PER_ROW;
+                        const uint4 val = ld_shared_v4(stage + sw128_offset(row, ch));
+                        if (row0 + row < N)
+                            *reinterpret_cast<uint4 *>(obase + (static_cast<size_t>(row) * D + ch * 8) *
+                                                                   sizeof(T)) = val;
+                    }
+                }
+                mbar_arrive(bar(C::B_QEMPTY + h));  // the next item's Q_h may land
             }
             // the staging tile is free again; stop together if anything failed
-            if constexpr (C::STAGE_IN_Q)
-                mbar_arrive(bar(C::B_QEMPTY + h));  // the next item's Q_h may land
             if (named_bar_or(1 + h, 4 * 32, bad || *abort_flag != 0))
                 break;
             done += nkh;
