@@ -26,8 +26,10 @@
 //                (tcgen05.mma, fp32 accumulators in TMEM).  V is an MN-major
 //                B operand.
 //   warps 4h..4h+3  softmax warpgroup of sub-tile h: thread t owns query row t
-//                = TMEM lane t.  It loads S, masks, takes the row max, updates
-//                the reference max, rescales l and O (in TMEM) by alpha, forms
+//                = TMEM lane t.  It loads S, masks, takes the row max (D <= 64,
+//                non-causal: only when the tile's sum shows the reference may
+//                have to move), updates the reference max, rescales l and O
+//                (in TMEM) by alpha, forms
 //                p = 2^(s*c - m*c) with one FMA + ex2, sums l in fp32, rounds P
 //                to the input dtype (D <= 64: in the same loop) into TMEM, and
 //                finally stages O / l in shared memory (D <= 64: one TMA
@@ -58,12 +60,13 @@ constexpr int kBN = 128;            // keys per K/V tile
 // warpgroup (warps 8 and 10 MMA issuers of sub-tiles 0 and 1, warp 9 TMA
 // producer, warp 11 idle).
 // Launched at 168 registers per thread (384 x 168 = 64512); the control
-// warpgroup drops to 96 and the softmax warpgroups rise to 200:
-// 256 x 200 + 128 x 96 = 63488 <= 64512.
+// warpgroup drops to 72 and the softmax warpgroups rise to 216 for the
+// non-causal D <= 64 launch (96 and 200 otherwise, measured faster there):
+// 256 x 216 + 128 x 72 = 64512.
 constexpr int kNumThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-constexpr uint32_t kRegsSoftmax = 216;  // d <= 64, non-causal (otherwise 200: measured faster there)
+constexpr uint32_t kRegsSoftmax = 216;  // D <= 64, non-causal (S and P of a tile live at once)
 constexpr uint32_t kRegsControl = 72;
 constexpr uint32_t kRegsSoftmaxWide = 200;
 constexpr uint32_t kRegsControlWide = 96;
@@ -92,6 +95,7 @@ __host__ __device__ constexpr int col_blocks()
     return (D + 63) / 64;
 }
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleBound = 256.0f;  // 2^kRescaleLog2
 
 template <int D>
 struct KCfg {
@@ -600,23 +604,51 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 uint32_t pw[64];  // P_h,j rounded to the input dtype, two per word
                 if constexpr (EARLY_S) {
                     // S_h,j is in registers: let the next S_h product in now, so
-                    // that it runs during this tile's exponentials.  The row max
-                    // comes first, so no tile is ever redone from S.
+                    // that it runs during this tile's exponentials.
                     tc_fence_before();
                     mbar_arrive(bar(C::B_SFREE + h));
-                    const float mt = row_max(s);
-                    if (j == 0) {
-                        m_ref = mt;
-                        alpha = 0.f;
-                    } else {
-                        const bool grow = (mt - m_ref) * scale_log2 > kRescaleLog2;
-                        if (__any_sync(0xffffffffu, grow) && grow) {
-                            alpha = ex2_approx((m_ref - mt) * scale_log2);
+                    if (CAUSAL || j == 0) {
+                        // causal: the row max first (its launch keeps the
+                        // smaller register budget, which the check's second
+                        // copy of the tile would exceed)
+                        const float mt = row_max(s);
+                        if (j == 0) {
                             m_ref = mt;
+                            alpha = 0.f;
+                        } else {
+                            const bool grow = (mt - m_ref) * scale_log2 > kRescaleLog2;
+                            if (__any_sync(0xffffffffu, grow) && grow) {
+                                alpha = ex2_approx((m_ref - mt) * scale_log2);
+                                m_ref = mt;
+                            }
+                        }
+                        rsum = masked ? exp_pack_tile<true, T>(s, pw, limit, scale_log2, -m_ref * scale_log2)
+                                      : exp_pack_tile<false, T>(s, pw, limit, scale_log2, -m_ref * scale_log2);
+                    } else {
+                        // Against the current reference first.  The reference
+                        // must move only if some p exceeds 2^kRescaleLog2, and
+                        // the largest p is at most the row sum, so the row max
+                        // is needed only when the sum exceeds that bound (or is
+                        // not finite); the tile is then redone from the scores,
+                        // which are still in registers.  Same results as taking
+                        // the row max first.
+                        rsum = masked ? exp_pack_tile<true, T>(s, pw, limit, scale_log2, -m_ref * scale_log2)
+                                      : exp_pack_tile<false, T>(s, pw, limit, scale_log2, -m_ref * scale_log2);
+                        const bool check = !(rsum <= kRescaleBound);
+                        if (__any_sync(0xffffffffu, check)) {
+                            const float mt = row_max(s);
+                            const bool grow = (mt - m_ref) * scale_log2 > kRescaleLog2;
+                            if (__any_sync(0xffffffffu, grow)) {
+                                if (grow) {
+                                    alpha = ex2_approx((m_ref - mt) * scale_log2);
+                                    m_ref = mt;
+                                }
+                                rsum = masked
+                                           ? exp_pack_tile<true, T>(s, pw, limit, scale_log2, -m_ref * scale_log2)
+                                           : exp_pack_tile<false, T>(s, pw, limit, scale_log2, -m_ref * scale_log2);
+                            }
                         }
                     }
-                    rsum = masked ? exp_pack_tile<true, T>(s, pw, limit, scale_log2, -m_ref * scale_log2)
-                                  : exp_pack_tile<false, T>(s, pw, limit, scale_log2, -m_ref * scale_log2);
                 } else if (j == 0) {
                     m_ref = row_max(s);
                     alpha = 0.f;
