@@ -24,7 +24,7 @@ LIB = os.path.join(OUT_DIR, LIB_NAME)
 LIB_CHECKED = os.path.join(OUT_DIR, "libfa_gb300_checked.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa1_fwd_kernel.cuh",
-                                                  "fa_bwd_kernel.cuh", "fa_decode_kernel.cuh",
+                                                  "fa_bwd_kernel.cuh", "fa_decode_kernel.cuh", "fa_decode_tc_kernel.cuh",
                                                   "fa_common.cuh",
                                                   "fa_host.h", "sm100_ptx.cuh")] + [
     os.path.join(INCLUDE, "fa.h")]

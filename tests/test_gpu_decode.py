@@ -1,6 +1,8 @@
 """Decoding attention (fa_decode, split-KV) against the fp64 oracle through
-the C ABI, with the forward pass's tolerance (P stays fp32 here, so only the
-output rounding and fp32 sums enter); full checks at the bench sizes."""
+the C ABI, with the forward pass's tolerance (the CUDA-core path keeps P in
+fp32; the tensor-core path for 3-16 queries at d = 128 rounds P to the input
+type before the P V product, as the forward does); full checks at the bench
+sizes."""
 import numpy as np
 import pytest
 import torch
@@ -68,3 +70,32 @@ def test_workload_full(orc, name):
     """The bench's decoding workloads, every output row checked."""
     q, k, v, meta = inputs.make_decode_workload(name)
     check(orc, q, k, v, meta["d"] ** -0.5, meta["causal"], "decode workload %s" % name)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(3, 3), (3, 300), (4, 4097), (8, 1500), (15, 2000), (16, 129)])
+def test_tensor_core_path(orc, dtype, causal, Nq, Nk):
+    """d = 128 with 3-16 queries: both products on the tensor cores (queries
+    padded to 16, ragged key tails, one or several chunks per head)."""
+    q, k, v = inputs.make_decode(3, 5, Nq, Nk, 128, dtype, (9700 + Nk, 9800 + Nq, 9900))
+    check(orc, q, k, v, 128 ** -0.5, causal, "decode tc Nq%d Nk%d %s causal=%s" % (Nq, Nk, dtype, causal))
+
+
+def test_tensor_core_many_items(orc):
+    """More (head, chunk) items than SMs: every CTA runs several items, so the
+    Q buffers, the O accumulator hand-over and the ring wrap many times."""
+    q, k, v = inputs.make_decode(4, 40, 3, 3000, 128, "bf16", (9911, 9912, 9913))
+    check(orc, q, k, v, 128 ** -0.5, True, "decode tc many items")
+
+
+@pytest.mark.parametrize("Nq", [1, 4])
+def test_rising_scores(orc, Nq):
+    """Scores that grow along the keys (about 2 log2 units per 128-key tile):
+    the running reference moves again and again inside a chunk, so the
+    accumulated O and row sums are rescaled many times."""
+    q, k, v = inputs.make_decode(1, 3, Nq, 5000, 128, "fp16", (9921, 9922, 9923))
+    q = (q.float().abs() + 1.0).to(q.dtype)
+    ramp = torch.linspace(0.0, 3.0, 5000).view(1, 1, 5000, 1)
+    k = (k.float() + ramp).to(k.dtype)
+    check(orc, q, k, v, 128 ** -0.5, False, "decode rising Nq%d" % Nq)
