@@ -160,16 +160,22 @@ struct Cfg {
     static_assert(32 % DQ_COLS == 0, "a 32-column TMEM load covers whole chunks");
 };
 
-// Work item number w: (head bh, key block n).  Causal: the heaviest key
-// blocks (low n, which see the most query blocks) of every head first.
-// Non-causal: head-major, so CTAs running together share one head's Q and dO
-// in L2.
+// Work item number w: (head bh, key block n).  Causal: the heads go in
+// groups of hg (the last group may be smaller); inside a group the heaviest
+// key blocks (low n, which see the most query blocks) of every head come
+// first, so that the CTAs running at one time share the Q, dO and dQ
+// accumulator of a few heads in L2.  Non-causal: head-major, for the same
+// reason.
 template <bool CAUSAL>
-__device__ __forceinline__ void item_coords(int w, int BH, int nb, int &bh, int &n)
+__device__ __forceinline__ void item_coords(int w, int BH, int nb, int hg, int &bh, int &n)
 {
     if (CAUSAL) {
-        n = w / BH;
-        bh = w % BH;
+        const int g = w / (hg * nb);
+        const int h0 = g * hg;
+        const int gs = min(hg, BH - h0);  // heads in this group
+        const int r = w - h0 * nb;
+        n = r / gs;
+        bh = h0 + r % gs;
     } else {
         bh = w / nb;
         n = w % nb;
@@ -181,7 +187,7 @@ __device__ __forceinline__ void item_coords(int w, int BH, int nb, int &bh, int 
 // round in reverse CTA order, so that the heavy and light causal items of
 // consecutive rounds even out per CTA.  False past the last item.
 template <bool CAUSAL>
-__device__ __forceinline__ bool item_of(int k, int BH, int nb, int &bh, int &n)
+__device__ __forceinline__ bool item_of(int k, int BH, int nb, int hg, int &bh, int &n)
 {
     // (the host keeps BH * nb + gridDim.x within int range)
     const int G = static_cast<int>(gridDim.x);
@@ -189,7 +195,7 @@ __device__ __forceinline__ bool item_of(int k, int BH, int nb, int &bh, int &n)
     const int w = k * G + ((k & 1) ? G - 1 - cta : cta);
     if (w >= BH * nb)
         return false;
-    item_coords<CAUSAL>(w, BH, nb, bh, n);
+    item_coords<CAUSAL>(w, BH, nb, hg, bh, n);
     return true;
 }
 
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                   const __grid_constant__ CUtensorMap tm_dqacc, const float *__restrict__ lse2,
-                  const float *__restrict__ dvec, int N, int Npad, int BH, int nb, float scale,
+                  const float *__restrict__ dvec, int N, int Npad, int BH, int nb, int hg, float scale,
                   float scale_log2)
 {
     using C = Cfg<D>;
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             bool ok = true;
-            for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, bh, n); ++k) {
+            for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, hg, bh, n); ++k) {
                 const int m0 = CAUSAL ? n : 0;  // first query block that sees key block n
                 const int cnt = nb - m0;        // query blocks walked (>= 1)
                 // the first query block ahead of K_n, V_n: its ring slots free up
@@ -418,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             bool ok = true;
             int g = 0;
-            bool have = item_of<CAUSAL>(0, BH, nb, bh, n);
+            bool have = item_of<CAUSAL>(0, BH, nb, hg, bh, n);
             // the first item's first block (CONT: every later item's first
             // block starts inside the previous item's last block)
             if (have)
@@ -427,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int cnt = nb - (CAUSAL ? n : 0);
                 const int kb = k % KVBUF;
                 int bh1 = 0, n1 = 0;
-                const bool have_next = item_of<CAUSAL>(k + 1, BH, nb, bh1, n1);
+                const bool have_next = item_of<CAUSAL>(k + 1, BH, nb, hg, bh1, n1);
                 for (int i = 0; ok && i < cnt; ++i) {
                     const int gi = g + i;
                     const int s = gi % QST, ds = gi % DOST;
@@ -520,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = threadIdx.x == kDqWarp0 * 32;
         int chunk = 0, g = 0;
         bool ok = true;
-        for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, bh, n); ++k) {
+        for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, hg, bh, n); ++k) {
             const int m0 = CAUSAL ? n : 0;
             const int cnt = nb - m0;
             for (int i = 0; i < cnt; ++i) {
@@ -636,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 c2 = make_float2(scale_log2, scale_log2);
         bool ok = true;
         int g = 0;
-        for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, bh, n); ++k) {
+        for (int k = 0; ok && item_of<CAUSAL>(k, BH, nb, hg, bh, n); ++k) {
             const int m0 = CAUSAL ? n : 0;
             const int cnt = nb - m0;
             const bool row_valid = n * kBlk + r < N;
