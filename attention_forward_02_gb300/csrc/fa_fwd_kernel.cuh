@@ -718,8 +718,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
 
             // ---------------- epilogue of sub-tile h ----------------
-            // Both named barriers below are reached by all four warps, whatever
+            // The named barriers below are reached by all four warps, whatever
             // happened; their OR-reductions give every warp the same decision.
+            if constexpr (!C::STAGE_IN_Q) {
+                // the previous item's tensor store has read the staging tile
+                // (waited for here, an item later, rather than right after it)
+                if (r == 0)
+                    bulk_wait_group_read<0>();
+                named_bar_sync(1 + h, 4 * 32);
+            }
             if (ok) {
                 ok = wait_warp(bar(C::B_OFINAL + h), it & 1, abort_flag);
             }
@@ -769,7 +776,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     for (int b = 0; b < col_blocks<D>(); ++b)
                         tma_store_3d(&tm_o, stage + b * kSwAtomBytes, b * 64, row0, bh);
                     bulk_commit_group();
-                    bulk_wait_group_read<0>();  // the staging tile has been read
                 }
             } else {
                 // O staged in Q_h: the warpgroup copies it out itself (16-byte
@@ -791,11 +797,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 mbar_arrive(bar(C::B_QEMPTY + h));  // the next item's Q_h may land
             }
-            // the staging tile is free again; stop together if anything failed
+            // stop together if anything failed (D > 64: the copy-out has read
+            // the staging tile, which the next item's Q may now overwrite)
             if (named_bar_or(1 + h, 4 * 32, bad || *abort_flag != 0))
                 break;
             done += nkh;
             Lr += 2 * nk_sub(qb, 1);
+        }
+        if constexpr (!C::STAGE_IN_Q) {
+            if (r == 0)
+                bulk_wait_group<0>();  // the last tensor store is complete
         }
         tc_fence_before();
     }

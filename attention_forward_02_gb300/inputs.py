@@ -79,6 +79,9 @@ def make_dout(B, H, N, d, dtype="fp16", seed=3):
 DECODE_WORKLOADS = {
     "decode": (8, 32, 1, 16384, 128, "fp16", (60, 61, 62), False),
     "decode_spec": (8, 32, 4, 16384, 128, "bf16", (63, 64, 65), True),
+    # decode_spec at a quarter of the heads (K/V 0.54 GB, still above L2): for
+    # multi-pass profiler captures, which save and restore device memory
+    "decode_spec_b2": (2, 32, 4, 16384, 128, "bf16", (69, 70, 71), True),
     # small case for the CPU tests of bench.py's decoding legs
     "decode_small": (1, 4, 2, 1024, 64, "fp16", (66, 67, 68), True),
 }
