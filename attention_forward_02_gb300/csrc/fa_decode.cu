@@ -1,7 +1,7 @@
 // fa_decode.cu -- host side of the decoding entry points declared in
 // include/fa.h: argument checks, the split-KV plan, TMA descriptors, and the
-// two launches (per-chunk partials on the CUDA cores, or on the tensor cores
-// for 3-16 queries at d = 128; then the combine).
+// two launches (per-chunk partials on the CUDA cores for a few queries, on
+// the tensor cores for more; then the combine).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,13 +45,23 @@ cudaError_t set_smem_attr_all()
     return e;
 }
 
+template <int D, typename T>
+cudaError_t set_smem_attr_tc()
+{
+    return cudaFuncSetAttribute(fa::dectc::fa_decode_tc_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                fa::dectc::Cfg<D>::SMEM_ALLOC);
+}
+
 void init_dec(DecState &st)
 {
-    cudaError_t e = cudaFuncSetAttribute(fa::dectc::fa_decode_tc_kernel<__half>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, fa::dectc::Cfg::SMEM_ALLOC);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fa::dectc::fa_decode_tc_kernel<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, fa::dectc::Cfg::SMEM_ALLOC);
+    cudaError_t e = set_smem_attr_tc<32, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_tc<64, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_tc<96, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_tc<128, __half>();
+    if (e == cudaSuccess) e = set_smem_attr_tc<32, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_tc<64, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_tc<96, __nv_bfloat16>();
+    if (e == cudaSuccess) e = set_smem_attr_tc<128, __nv_bfloat16>();
     if (e == cudaSuccess) e = set_smem_attr_all<32, __half>();
     if (e == cudaSuccess) e = set_smem_attr_all<64, __half>();
     if (e == cudaSuccess) e = set_smem_attr_all<96, __half>();
@@ -102,13 +112,16 @@ fa_status_t launch_nq(const CUtensorMap &mk, const CUtensorMap &mv, const void *
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-// Q of the tensor-core path as [BH, Nq, 128] 16-bit: one box is 16 query rows
-// x 64 columns (rows past Nq read as zeros), 128B-swizzled, the K-major
-// operand of S^T = K Q^T.
-fa_status_t encode_q16_map(EncodeTiledFn encode, CUtensorMap *map, const void *q, int BH, int Nq, fa_dtype_t dtype)
+bool use_tensor_cores(int Nq, int d) { return Nq >= (d >= 96 ? 3 : 5); }
+
+// Q of the tensor-core path as [BH, Nq, d] 16-bit: one box is 16 query rows
+// x 64 columns (rows past Nq and columns past d read as zeros), 128B-swizzled,
+// the K-major operand of S^T = K Q^T.
+fa_status_t encode_q16_map(EncodeTiledFn encode, CUtensorMap *map, const void *q, int BH, int Nq, int d,
+                           fa_dtype_t dtype)
 {
-    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(Nq), static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(Nq) * 128 * 2};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Nq), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Nq) * d * 2};
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(fa::dectc::kNP), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = encode(map, dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -118,8 +131,8 @@ fa_status_t encode_q16_map(EncodeTiledFn encode, CUtensorMap *map, const void *q
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// 2-16 queries at head dim 128: both products on the tensor cores.
-template <typename T>
+// 3-16 queries: both products on the tensor cores.
+template <int D, typename T>
 fa_status_t launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, void *o, float *lse,
                       float *ws, int BH, int Nq, int Nk, float scale, int causal, int num_sms, cudaStream_t stream)
 {
@@ -128,15 +141,15 @@ fa_status_t launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtens
     plan(BH, Nk, num_sms, &splits, &per);
     Partials part;
     part.o = ws;
-    part.m = ws + static_cast<size_t>(BH) * splits * Nq * 128;
+    part.m = ws + static_cast<size_t>(BH) * splits * Nq * D;
     part.l = part.m + static_cast<size_t>(BH) * splits * Nq;
     const int items = BH * splits;
     const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    fa::dectc::fa_decode_tc_kernel<T><<<grid, fa::dectc::kThreads, fa::dectc::Cfg::SMEM_ALLOC, stream>>>(
+    fa::dectc::fa_decode_tc_kernel<D, T><<<grid, fa::dectc::kThreads, fa::dectc::Cfg<D>::SMEM_ALLOC, stream>>>(
         mq, mk, mv, part, Nq, Nk, splits, per, items, causal, scale_log2);
     const long long rows = static_cast<long long>(BH) * Nq;
-    fa::dec::fa_decode_combine_kernel<128, T><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+    fa::dec::fa_decode_combine_kernel<D, T><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
         part, static_cast<T *>(o), lse, rows, Nq, splits);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -254,15 +267,24 @@ fa_status_t fa_decode(const void *q, const void *k, const void *v, void *o, floa
     if ((s = fa_host::encode_qkv_map(encode, &mv, v, bh, Nk, d, dtype)) != FA_OK) return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     float *ws = static_cast<float *>(workspace);
-    // 3-16 queries at d = 128: the tensor-core kernel (at 2 queries the
-    // CUDA-core one still keeps up with HBM and is slightly faster)
-    if (d == 128 && Nq >= 3) {
+    // The tensor-core kernel from 3 queries on at d >= 96 and from 5 on at
+    // d <= 64 (measured: at 1 or 2 queries, and at 3 or 4 with d <= 64, the
+    // CUDA-core kernel is faster; beyond, its query loops grow with Nq)
+    if (use_tensor_cores(Nq, d)) {
         CUtensorMap mq;
-        if ((s = encode_q16_map(encode, &mq, q, bh, Nq, dtype)) != FA_OK)
+        if ((s = encode_q16_map(encode, &mq, q, bh, Nq, d, dtype)) != FA_OK)
             return s;
-        if (dtype == FA_FP16)
-            return launch_tc<__half>(mq, mk, mv, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs);
-        return launch_tc<__nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs);
+#define FA_DEC_TC(DD)                                                                                      \
+    if (d == DD)                                                                                           \
+        return dtype == FA_FP16                                                                            \
+                   ? launch_tc<DD, __half>(mq, mk, mv, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs)     \
+                   : launch_tc<DD, __nv_bfloat16>(mq, mk, mv, o, lse, ws, bh, Nq, Nk, scale, causal, sms, cs);
+        FA_DEC_TC(32)
+        FA_DEC_TC(64)
+        FA_DEC_TC(96)
+        FA_DEC_TC(128)
+#undef FA_DEC_TC
+        return FA_ERR_UNSUPPORTED;
     }
 #define FA_DEC_D(DD, TT)                                                                                  \
     if (d == DD)                                                                                          \

@@ -1,5 +1,5 @@
-// fa_decode_tc_kernel.cuh -- decoding attention for 2 <= Nq <= 16 queries at
-// head dim 128, with the two products on the tensor cores.
+// fa_decode_tc_kernel.cuh -- decoding attention for 3 <= Nq <= 16 queries,
+// with the two products on the tensor cores.
 //
 // It computes what fa_decode_split_kernel computes (the same split-KV items,
 // the same per-chunk partials m, l, O for fa_decode_combine_kernel): the
@@ -10,9 +10,11 @@
 // the products than HBM needs to deliver K and V; here, per tile,
 //   S^T = K Q^T    tcgen05.mma M = 128 keys, N = 16 (queries, zero-padded),
 //                  K = d; A = the K tile (K-major), B = the Q tile (K-major)
-//   O^T += V^T P^T tcgen05.mma M = 128 (d), N = 16, K = 128 keys; A = the V
-//                  tile read MN-major (no transpose copy), B = P^T written to
-//                  shared memory by the softmax warps
+//   O^T += V^T P^T tcgen05.mma M = 128 (d, zero-padded: the V tile always
+//                  has two 64-column blocks, and the columns past d hold
+//                  zeros), N = 16, K = 128 keys; A = the V tile read MN-major
+//                  (no transpose copy), B = P^T written to shared memory by
+//                  the softmax warps
 // with fp32 accumulators in TMEM (S^T in two buffers, so the next tile's
 // product runs while this tile's softmax does).
 //
@@ -32,7 +34,6 @@
 namespace fa {
 namespace dectc {
 
-constexpr int kD = 128;
 constexpr int kKeys = 128;       // keys per tile
 constexpr int kNP = 16;          // queries per product (Nq padded)
 constexpr int kThreads = 192;
@@ -42,14 +43,20 @@ constexpr uint32_t kTmemCols = 64;  // S^T buffers at 0 and 16, O^T at 32
 constexpr uint32_t kTmO = 32;
 constexpr float kRescaleLog2 = 8.0f;
 
+template <int D>
 struct Cfg {
-    static constexpr int TILE = kKeys * kD * 2;        // one K or V tile: two 16 KB swizzle blocks
-    static constexpr int STAGES = 3;
+    static_assert(D == 32 || D == 64 || D == 96 || D == 128, "head dims 32, 64, 96, 128");
+    static constexpr int CB = (D + 63) / 64;            // 64-column blocks of a K, V or Q row
+    static constexpr int KTILE = kKeys * CB * 128;      // one K tile (TMA fills columns past D with zeros)
+    static constexpr int VTILE = kKeys * 2 * 128;       // one V tile: always two blocks (M = 128); with
+                                                        // D <= 64 the second holds zeros, written once
+    static constexpr int STAGE = KTILE + VTILE;
+    static constexpr int STAGES = D <= 64 ? 4 : 3;
     static constexpr int QBLK = kNP * 128;              // one 64-column block of the Q tile (16 rows x 128 B)
-    static constexpr int QTILE = 2 * QBLK;              // [16 x 128] 16-bit
+    static constexpr int QTILE = CB * QBLK;             // [16 x 64 CB] 16-bit
     static constexpr int PTILE = 2 * QBLK;              // P^T [16 queries x 128 keys] 16-bit
-    static constexpr int KV_OFF = 0;                    // stage s: K at 2 s TILE, V at (2 s + 1) TILE
-    static constexpr int Q_OFF = KV_OFF + STAGES * 2 * TILE;  // two Q tiles (item parity)
+    static constexpr int KV_OFF = 0;                    // stage s: K at s STAGE, V at s STAGE + KTILE
+    static constexpr int Q_OFF = KV_OFF + STAGES * STAGE;  // two Q tiles (item parity)
     static constexpr int P_OFF = Q_OFF + 2 * QTILE;           // two P^T tiles (tile parity)
     static constexpr int RED_OFF = P_OFF + 2 * PTILE;          // fp32 [2][4 warps][16] maxima
     static constexpr int LSUM_OFF = RED_OFF + 2 * 4 * kNP * 4; // fp32 [4 warps][16] row sums
@@ -69,7 +76,9 @@ struct Cfg {
     static constexpr int SMEM_USED = SLOT_OFF + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-    static_assert(QBLK % 1024 == 0 && Q_OFF % 1024 == 0 && P_OFF % 1024 == 0, "1024-byte aligned operand tiles");
+    static_assert(QBLK % 1024 == 0 && Q_OFF % 1024 == 0 && P_OFF % 1024 == 0 && STAGE % 1024 == 0 &&
+                      KTILE % 1024 == 0,
+                  "1024-byte aligned operand tiles");
 };
 
 // Byte offset of 16-bit element (row, col) of a [16 rows x 128] tile stored as
@@ -78,7 +87,7 @@ struct Cfg {
 __device__ __forceinline__ uint32_t small_tile_offset(int row, int col)
 {
     const int chunk = (col & 63) >> 3;
-    return static_cast<uint32_t>((col >> 6) * Cfg::QBLK + row * 128 + (((chunk ^ (row & 7)) << 4)) + (col & 7) * 2);
+    return static_cast<uint32_t>((col >> 6) * (kNP * 128) + row * 128 + (((chunk ^ (row & 7)) << 4)) + (col & 7) * 2);
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
@@ -95,15 +104,15 @@ __device__ __forceinline__ uint16_t to16(float x)
     return static_cast<uint16_t>(w & 0xFFFFu);
 }
 
-template <typename T>
+template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, dec::Partials part, int Nq, int Nk, int splits,
                         int tiles_per_split, int num_items, int causal, float scale_log2)
 {
-    using C = Cfg;
+    using C = Cfg<D>;
     constexpr int STAGES = C::STAGES;
-    constexpr int KSTEPS = kD / 16;     // S^T: K = d
+    constexpr int KSTEPS = D / 16;      // S^T: K = d
     constexpr int PSTEPS = kKeys / 16;  // O^T: K = keys
 
     extern __shared__ uint8_t smem_raw[];
@@ -150,6 +159,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
         tmem_relinquish();
     }
+    if constexpr (C::CB == 1) {
+        // the second 64-column block of every V tile: zeros for the O^T
+        // product's rows past D (no load ever writes it)
+        if (warp < 4) {
+            for (int i = threadIdx.x; i < STAGES * (kSwAtomBytes / 16); i += 128) {
+                const int st = i / (kSwAtomBytes / 16), ch = i % (kSwAtomBytes / 16);
+                st_shared_v4(sbase + C::KV_OFF + st * C::STAGE + C::KTILE + kSwAtomBytes + ch * 16, 0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // read by the tensor core
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -172,19 +192,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (items >= 2 && !(ok = wait_bounded(bar(C::B_QEMPTY + qb), ((items / 2) - 1) & 1, abort_flag)))
                     break;
                 mbar_arrive_expect_tx(bar(C::B_QFULL + qb), C::QTILE);
-                for (int b = 0; b < 2; ++b)
+                for (int b = 0; b < C::CB; ++b)
                     tma_load_3d(sbase + C::Q_OFF + qb * C::QTILE + b * C::QBLK, &tm_q, bar(C::B_QFULL + qb),
                                 b * 64, 0, bh, pol);
                 for (int i = 0; i < nt; ++i, ++L) {
                     const int s = L % STAGES;
                     if (L >= STAGES && !(ok = wait_bounded(bar(C::B_EMPTY + s), ((L / STAGES) - 1) & 1, abort_flag)))
                         break;
-                    const uint32_t kdst = sbase + C::KV_OFF + (2 * s) * C::TILE;
-                    mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::TILE);
-                    for (int b = 0; b < 2; ++b) {
+                    const uint32_t kdst = sbase + C::KV_OFF + s * C::STAGE;
+                    mbar_arrive_expect_tx(bar(C::B_FULL + s), 2 * C::CB * kSwAtomBytes);
+                    for (int b = 0; b < C::CB; ++b) {
                         tma_load_3d(kdst + b * kSwAtomBytes, &tm_k, bar(C::B_FULL + s), b * 64, (t0 + i) * kKeys,
                                     bh, pol);
-                        tma_load_3d(kdst + C::TILE + b * kSwAtomBytes, &tm_v, bar(C::B_FULL + s), b * 64,
+                        tma_load_3d(kdst + C::KTILE + b * kSwAtomBytes, &tm_v, bar(C::B_FULL + s), b * 64,
                                     (t0 + i) * kKeys, bh, pol);
                     }
                 }
@@ -204,9 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tile g - 1 (whose P^T the softmax writes meanwhile).
             constexpr bool BF = DTypeTraits<T>::kBF16;
             constexpr uint32_t idesc_s = make_idesc_f16(BF, kKeys, kNP, false, false);
-            constexpr uint32_t idesc_o = make_idesc_f16(BF, kD, kNP, true, false);
+            constexpr uint32_t idesc_o = make_idesc_f16(BF, 128, kNP, true, false);
             const uint64_t desc_k0 = make_sdesc_sw128(sbase + C::KV_OFF, 16, 1024);
-            const uint64_t desc_v0 = make_sdesc_sw128(sbase + C::KV_OFF + C::TILE, kSwAtomBytes, 1024);
+            const uint64_t desc_v0 = make_sdesc_sw128(sbase + C::KV_OFF + C::KTILE, kSwAtomBytes, 1024);
             const uint64_t desc_q0 = make_sdesc_sw128(sbase + C::Q_OFF, 16, 1024);
             const uint64_t desc_p0 = make_sdesc_sw128(sbase + C::P_OFF, 16, 1024);
             // the O^T product of global tile gp (item-local tile jp, CTA item ip)
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 tc_fence_after();
                 const int s = gp % STAGES;
-                const uint64_t vd = desc_v0 + static_cast<uint32_t>((s * 2 * C::TILE) >> 4);
+                const uint64_t vd = desc_v0 + static_cast<uint32_t>((s * C::STAGE) >> 4);
                 const uint64_t pd = desc_p0 + static_cast<uint32_t>((b * C::PTILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < PSTEPS; ++kk) {
@@ -253,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok)
                         break;
                     tc_fence_after();
-                    const uint64_t kd = desc_k0 + static_cast<uint32_t>((s * 2 * C::TILE) >> 4);
+                    const uint64_t kd = desc_k0 + static_cast<uint32_t>((s * C::STAGE) >> 4);
                     const uint64_t qd = desc_q0 + static_cast<uint32_t>((qb * C::QTILE) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -406,10 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(C::B_OFREE));  // the next item's first product may overwrite O^T
             const size_t base = (static_cast<size_t>(bh) * splits + split) * Nq;
+            if (t < D) {
 #pragma unroll
-            for (int q = 0; q < kNP; ++q)
-                if (q < Nq)
-                    part.o[(base + q) * kD + t] = __uint_as_float(ou[q]);
+                for (int q = 0; q < kNP; ++q)
+                    if (q < Nq)
+                        part.o[(base + q) * D + t] = __uint_as_float(ou[q]);
+            }
             if (t < Nq) {
                 float lq = 0.f, mq = 0.f;
 #pragma unroll
