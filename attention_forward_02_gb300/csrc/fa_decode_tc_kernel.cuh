@@ -318,49 +318,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nt; ++j, ++g) {
                 const int b = g & 1;
                 ok = wait_warp(bar(C::B_SFULL + b), static_cast<uint32_t>((g >> 1) & 1), abort_flag);
-                if (named_bar_or(1, 128, !ok || *abort_flag != 0)) {
-                    ok = false;
-                    break;
-                }
                 tc_fence_after();
                 uint32_t su[kNP];
-                tmem_ld16(tmem + lane_base + b * kNP, su);
+                tmem_ld16(tmem + lane_base + b * kNP, su);  // (read whatever the wait gave)
                 tc_fence_before();
-                mbar_arrive(bar(C::B_SFREE + b));
+                if (ok)
+                    mbar_arrive(bar(C::B_SFREE + b));
                 // scaled scores of key t (log2 units); masked: keys past the
                 // last one query q may see, and the padding queries
                 const int key = (t0 + j) * kKeys + t;
                 float x[kNP];
+                bool grow = false;  // some score of this thread outgrows its query's reference
 #pragma unroll
                 for (int q = 0; q < kNP; ++q) {
                     const int last = causal ? Nk - Nq + q : Nk - 1;
                     x[q] = (q < Nq && key <= last) ? __uint_as_float(su[q]) * scale_log2 : -INFINITY;
+                    grow = grow || (x[q] - m_ref[q] > kRescaleLog2);  // (-inf: never; reference -inf: any visible key)
                 }
-                // tile maxima per query: warp shuffles, then the four warps
-                float* rb = red + b * 4 * kNP;
-#pragma unroll
-                for (int q = 0; q < kNP; ++q) {
-                    float v = x[q];
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-                    if (lane == 0)
-                        rb[warp * kNP + q] = v;
-                }
-                named_bar_sync(1, 128);
-                // (every thread computes the same maxima and references)
+                // The references move only when a score outgrows one by more than
+                // 2^kRescaleLog2 (the first visible key of a query always does):
+                // one barrier tells every thread whether any did, or whether the
+                // CTA stops; only then are the tile's maxima exchanged.
                 float alpha[kNP];
-                bool moved = false;  // an earlier reference moved: O^T is rescaled
 #pragma unroll
-                for (int q = 0; q < kNP; ++q) {
-                    const float tmax = fmaxf(fmaxf(rb[q], rb[kNP + q]), fmaxf(rb[2 * kNP + q], rb[3 * kNP + q]));
+                for (int q = 0; q < kNP; ++q)
                     alpha[q] = 1.f;
-                    // the reference moves on the first visible key and when the
-                    // tile's max outgrows it by more than 2^kRescaleLog2
-                    if (tmax != -INFINITY && (m_ref[q] == -INFINITY || tmax - m_ref[q] > kRescaleLog2)) {
-                        moved = moved || (j > 0 && m_ref[q] != -INFINITY);
-                        alpha[q] = m_ref[q] == -INFINITY ? 0.f : ex2_approx(m_ref[q] - tmax);
-                        m_ref[q] = tmax;
+                bool moved = false;  // an earlier reference moved: O^T is rescaled
+                if (named_bar_or(1, 128, !ok || *abort_flag != 0 || grow)) {
+                    if (named_bar_or(1, 128, !ok || *abort_flag != 0)) {
+                        ok = false;
+                        break;
+                    }
+                    // tile maxima per query: warp shuffles, then the four warps
+                    float *rb = red + b * 4 * kNP;
+#pragma unroll
+                    for (int q = 0; q < kNP; ++q) {
+                        float v = x[q];
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                        if (lane == 0)
+                            rb[warp * kNP + q] = v;
+                    }
+                    named_bar_sync(1, 128);
+                    // (every thread computes the same maxima and references)
+#pragma unroll
+                    for (int q = 0; q < kNP; ++q) {
+                        const float tmax =
+                            fmaxf(fmaxf(rb[q], rb[kNP + q]), fmaxf(rb[2 * kNP + q], rb[3 * kNP + q]));
+                        // the reference moves on the first visible key and when the
+                        // tile's max outgrows it by more than 2^kRescaleLog2
+                        if (tmax != -INFINITY && (m_ref[q] == -INFINITY || tmax - m_ref[q] > kRescaleLog2)) {
+                            moved = moved || (j > 0 && m_ref[q] != -INFINITY);
+                            alpha[q] = m_ref[q] == -INFINITY ? 0.f : ex2_approx(m_ref[q] - tmax);
+                            m_ref[q] = tmax;
+                        }
                     }
                 }
                 float p[kNP];
