@@ -112,7 +112,7 @@ fa_status_t launch_nq(const CUtensorMap &mk, const CUtensorMap &mv, const void *
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-bool use_tensor_cores(int Nq, int d) { return Nq >= (d >= 96 ? 3 : 5); }
+bool use_tensor_cores(int Nq, int d) { return Nq >= 3 || (Nq == 2 && d == 128); }
 
 // Q of the tensor-core path as [BH, Nq, d] 16-bit: one box is 16 query rows
 // x 64 columns (rows past Nq and columns past d read as zeros), 128B-swizzled,
@@ -267,9 +267,9 @@ fa_status_t fa_decode(const void *q, const void *k, const void *v, void *o, floa
     if ((s = fa_host::encode_qkv_map(encode, &mv, v, bh, Nk, d, dtype)) != FA_OK) return s;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     float *ws = static_cast<float *>(workspace);
-    // The tensor-core kernel from 3 queries on at d >= 96 and from 5 on at
-    // d <= 64 (measured: at 1 or 2 queries, and at 3 or 4 with d <= 64, the
-    // CUDA-core kernel is faster; beyond, its query loops grow with Nq)
+    // The tensor-core kernel from 3 queries on, and from 2 at d = 128
+    // (measured: with one query, and with two at d < 128, the CUDA-core
+    // kernel is as fast or faster; beyond, its query loops grow with Nq)
     if (use_tensor_cores(Nq, d)) {
         CUtensorMap mq;
         if ((s = encode_q16_map(encode, &mq, q, bh, Nq, d, dtype)) != FA_OK)

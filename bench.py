@@ -1223,7 +1223,7 @@ def run_decode_op(args, world, rank, local):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic,
                 "kernel": ("fa_decode_tc_kernel<%d,%s> + combine" % (d, meta["dtype"])
-                           if Nq >= (3 if d >= 96 else 5) else
+                           if Nq >= 3 or (Nq == 2 and d == 128) else
                            "fa_decode_split_kernel<%d,%s> + combine" % (d, meta["dtype"])),
                 "timed": "the whole fa_decode call (split kernel + combine kernel)",
                 "peak_source": "%s hbm_gbs (STREAM-style copy)" % peak_src,

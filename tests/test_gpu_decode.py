@@ -1,6 +1,6 @@
 """Decoding attention (fa_decode, split-KV) against the fp64 oracle through
 the C ABI, with the forward pass's tolerance (the CUDA-core path keeps P in
-fp32; the tensor-core path for 3-16 queries rounds P to the input
+fp32; the tensor-core path (3-16 queries, 2 at d = 128) rounds P to the input
 type before the P V product, as the forward does); full checks at the bench
 sizes."""
 import numpy as np
@@ -74,9 +74,10 @@ def test_workload_full(orc, name):
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("Nq,Nk", [(3, 3), (3, 300), (4, 4097), (8, 1500), (15, 2000), (16, 129)])
+@pytest.mark.parametrize("Nq,Nk", [(2, 2), (2, 300), (3, 3), (3, 300), (4, 4097), (8, 1500), (15, 2000),
+                                   (16, 129)])
 def test_tensor_core_path(orc, dtype, causal, Nq, Nk):
-    """d = 128 with 3-16 queries: both products on the tensor cores (queries
+    """d = 128 with 2-16 queries: both products on the tensor cores (queries
     padded to 16, ragged key tails, one or several chunks per head)."""
     q, k, v = inputs.make_decode(3, 5, Nq, Nk, 128, dtype, (9700 + Nk, 9800 + Nq, 9900))
     check(orc, q, k, v, 128 ** -0.5, causal, "decode tc Nq%d Nk%d %s causal=%s" % (Nq, Nk, dtype, causal))
@@ -87,10 +88,9 @@ def test_tensor_core_path(orc, dtype, causal, Nq, Nk):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Nq,Nk", [(3, 300), (5, 700), (8, 1500), (16, 129)])
 def test_tensor_core_path_head_dims(orc, dtype, d, causal, Nq, Nk):
-    """Head dims below 128 (the tensor-core kernel from 3 queries on at d = 96,
-    from 5 on at d <= 64; the CUDA-core kernel below): K = d in the score
-    product; the O^T product keeps M = 128 with the V tile's columns past d
-    zero (TMA zero-fills them for d = 96; a zeroed second block for d <= 64)."""
+    """Head dims below 128 on the tensor cores: K = d in the score product; the
+    O^T product keeps M = 128 with the V tile's columns past d zero (TMA
+    zero-fills them for d = 96; a zeroed second block for d <= 64)."""
     q, k, v = inputs.make_decode(2, 5, Nq, Nk, d, dtype, (9600 + Nk, 9650 + Nq, 9690 + d))
     check(orc, q, k, v, d ** -0.5, causal, "decode tc Nq%d Nk%d d%d %s causal=%s" % (Nq, Nk, d, dtype, causal))
 
