@@ -1,5 +1,6 @@
-// fa_decode_tc_kernel.cuh -- decoding attention for 3 <= Nq <= 16 queries,
-// with the two products on the tensor cores.
+// fa_decode_tc_kernel.cuh -- decoding attention for up to 16 queries per
+// head with the two products on the tensor cores (fa_decode uses it from 3
+// queries on, and from 2 at d = 128).
 //
 // It computes what fa_decode_split_kernel computes (the same split-KV items,
 // the same per-chunk partials m, l, O for fa_decode_combine_kernel): the
@@ -22,9 +23,10 @@
 // of S^T, dimension t of O^T), warp 4 TMA producer (Q once per item into one
 // of two buffers, K and V per tile through a ring), warp 5 MMA issuer (one
 // thread; also allocates TMEM).  The reference max of each query moves only
-// when a tile's max outgrows it by more than 2^8 (O^T and l are then
-// rescaled, as in the forward kernel); the partial m, l, O of a chunk are
-// consistent with whatever reference was used, which the combine step needs.
+// when one of its scores outgrows it by more than 2^8 (O^T and l are then
+// rescaled, as in the forward kernel); the tile's maxima are exchanged only
+// then.  The partial m, l, O of a chunk are consistent with whatever
+// reference was used, which the combine step needs.
 // Every mbarrier wait is bounded.
 #pragma once
 
