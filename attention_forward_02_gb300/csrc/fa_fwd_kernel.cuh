@@ -268,10 +268,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int lane = threadIdx.x & 31;
     const int num_items = BH * num_q_blocks;
     const int num_k_tiles = (N + kBN - 1) / kBN;
-    // key tiles of sub-tile h of Q block qb
-    auto nk_sub = [&](int qb, int h) {
-        return CAUSAL ? min(2 * qb + 1 + h, num_k_tiles) : num_k_tiles;
+    // key tiles of row half hr (rows qb kBM + hr kSubM ...) of Q block qb
+    auto nk_sub = [&](int qb, int hr) {
+        return CAUSAL ? min(2 * qb + 1 + hr, num_k_tiles) : num_k_tiles;
     };
+    // Causal: the lower row half sees one key tile more.  Sub-tile h takes row
+    // half h ^ swap_of(it), so the extra tile alternates between the two
+    // softmax warpgroups from one item of a CTA to the next and neither runs
+    // ahead of the other by more than a tile (the K/V ring would stop it).
+    auto swap_of = [](int it) { return CAUSAL ? (it & 1) : 0; };
 
     auto bar = [&](int idx) -> uint32_t {
         FA_CHECK(idx >= 0 && idx < C::NUM_BARS);
@@ -342,7 +347,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     mbar_arrive_expect_tx(bar(C::B_QFULL + qt0 + h), C::TILE);
                     for (int b = 0; b < col_blocks<D>(); ++b)
                         tma_load_3d(sbase + C::Q_OFF + (qt0 + h) * C::TILE + b * kSwAtomBytes, &tm_q,
-                                    bar(C::B_QFULL + qt0 + h), b * 64, qb * kBM + h * kSubM, bh, pol_q);
+                                    bar(C::B_QFULL + qt0 + h), b * 64, qb * kBM + (h ^ swap_of(it)) * kSubM, bh,
+                                    pol_q);
                 }
                 if (!ok)
                     break;
@@ -452,7 +458,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 int bh, qb;
                 item_coords<CAUSAL>(w, BH, num_q_blocks, bh, qb);
                 (void)bh;
-                const int nk0 = nk_sub(qb, 0), nk1 = nk_sub(qb, 1);
+                // key tiles of sub-tile 0 / 1, and of the longer one (the loads)
+                const int nk0 = nk_sub(qb, swap_of(it)), nk1 = nk_sub(qb, 1 ^ swap_of(it));
+                const int nkmax = nk_sub(qb, 1);
                 auto nk_of = [&](int h) { return h == 0 ? nk0 : nk1; };
                 auto done_of = [&](int h) { return h == 0 ? done0 : done1; };
                 qt0 = 2 * (it % C::QBUF);
@@ -473,7 +481,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 if constexpr (!EARLY_S)
                     release(0, true);
-                for (int j = 0; ok && j < nk1; ++j) {
+                for (int j = 0; ok && j < nkmax; ++j) {
                     if constexpr (EARLY_S) {
                         // next S products first, then this tile's P V products
                         for (int h = h_lo; ok && h < h_hi; ++h) {
@@ -529,7 +537,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                         if (ok)
                             ok = release(2 * j + 1, v_used);
-                        if (ok && j + 1 < nk1)
+                        if (ok && j + 1 < nkmax)
                             ok = release(2 * j + 2, k_used);
                     }
                 }
@@ -540,7 +548,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     umma_commit(bar(C::B_QEMPTY + qt0 + h));
                 done0 += nk0;
                 done1 += nk1;
-                Lb += 2 * nk1;
+                Lb += 2 * nkmax;
             }
             // every MMA this thread issued has completed once this arrives
             umma_commit(bar(C::B_DRAIN + me));
@@ -571,9 +579,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 break;
             int bh, qb;
             item_coords<CAUSAL>(w, BH, num_q_blocks, bh, qb);
-            const int row0 = qb * kBM + h * kSubM;
+            const int row0 = qb * kBM + (h ^ swap_of(it)) * kSubM;
             const int qrow = row0 + r;
-            const int nkh = nk_sub(qb, h);
+            const int nkh = nk_sub(qb, h ^ swap_of(it));
             float m_ref = -INFINITY;  // reference max (raw score units; scale >= 0)
             float l = 0.f;
             bool ok = true;
@@ -734,8 +742,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 tc_fence_after();
                 if (rel) {
                     kv_free(2 * nkh - 1);  // the last P V product has read V
-                    // key tiles this sub-tile skips (causal, sub-tile 0): freed
-                    // once they have landed (so that no slot is freed early)
+                    // key tiles this sub-tile skips (causal, the upper row
+                    // half): freed once they have landed (so that no slot is
+                    // freed early)
                     const int nk1 = nk_sub(qb, 1);
                     for (int ll = 2 * nkh; ok && ll < 2 * nk1; ++ll) {
                         const int L = Lr + ll;
