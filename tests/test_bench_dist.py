@@ -90,3 +90,5 @@ def test_decode_reference_arm_under_torchrun_prints_once():
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["metric"].startswith("decoding attention") and rec["unit"] == "GB/s"
     assert rec["config"]["Nq"] == 2 and rec["config"]["Nk"] == 1024
+    # a K/V cache this small (1 MB) sits in L2: its steps are timed after a flush
+    assert rec["config"]["l2"].startswith("flushed")
